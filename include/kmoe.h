@@ -1,0 +1,194 @@
+/*
+ * kmoe -- Kimi-K3 routed-expert MoE forward (MXFP8 activations x MXFP4
+ * weights, SiTU gated activation) for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument is a DEVICE pointer owned by the caller
+ * unless its comment says "host".  The library never allocates device
+ * memory and never synchronises the host inside these calls: work is
+ * enqueued on the given stream and errors that only the device can see
+ * (a bounded wait that gave up) are recorded in the workspace and read
+ * back with kmoe_device_error().  Argument errors are reported before
+ * anything is enqueued.  All calls are safe to capture in a CUDA graph
+ * (fixed grids, device-side counts, no host reads of device data).
+ *
+ * Layout conventions (all row-major, contiguous, no strides):
+ *   bf16 activations x      [T, H]
+ *   router logits           [T, E] float
+ *   correction bias         [E] float
+ *   w13 codes               [E, 2I, H/2] uint8, two E2M1 codes per byte
+ *                           (element 2j in the low nibble); rows [0, I) are
+ *                           the gate projection, rows [I, 2I) the up
+ *                           projection ("[gate; up]" halves)
+ *   w13 scales (raw)        [E, 2I, H/32] uint8 UE8M0 (value 2^(b-127))
+ *   w2 codes                [E, H, I/2] uint8
+ *   w2 scales (raw)         [E, H, I/32] uint8
+ *   output                  [T, H] bf16
+ * Sources (web pages this library follows):
+ *   - Kimi-K3 SM120 FlashInfer MXFP4 page: serving call chain (sigmoid +
+ *     correction-bias top-16 with renormalised weights), real checkpoint
+ *     contract (packed MXFP4, group-32 E8M0 scales, [gate; up] halves),
+ *     the SiTU formula with situ_beta = 4 and situ_linear_beta = 25, the
+ *     gated width rule (FC1 = 2 x FC2 K), the NaN/Inf decision record
+ *     (saturating-finite MXFP8, no 0xFF scale), and the non-fused,
+ *     deterministic finalize.
+ *   - Kimi-K3 MoE path analysis page (SM100 section): MXFP8 pre-dispatch
+ *     quantisation (per-32 absmax -> UE8M0 -> E4M3, four scale bytes per
+ *     int32), weight/scale re-layout at load time for TMEM-staged scales,
+ *     routed_scaling_factor.
+ */
+#ifndef KMOE_H_
+#define KMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (the only definition of these values). */
+enum kmoe_status {
+  KMOE_OK = 0,
+  KMOE_ERR_ARG = 1,        /* null pointer, k > E, non-positive size, bad enum */
+  KMOE_ERR_SHAPE = 2,      /* H or I not a multiple of 128, FC1 width != 2 x FC2 K, ... */
+  KMOE_ERR_ALIGN = 3,      /* a pointer is not aligned as documented */
+  KMOE_ERR_ARCH = 4,       /* device is not sm_103 (GB300) or the kernels do not load */
+  KMOE_ERR_WORKSPACE = 5,  /* workspace null or smaller than kmoe_workspace_size() */
+  KMOE_ERR_CUDA = 6,       /* a CUDA runtime/driver call failed */
+  KMOE_ERR_TIMEOUT = 7,    /* a device-side bounded wait gave up (see kmoe_device_error) */
+  KMOE_ERR_DEVICE = 8      /* other device-side error (e.g. an expert id >= E in the input) */
+};
+
+/* Quantisation formats for kmoe_quantize_mx. */
+enum kmoe_mx_format {
+  KMOE_MXFP8_E4M3 = 0,  /* one E4M3 code per byte */
+  KMOE_MXFP4_E2M1 = 1   /* two E2M1 codes per byte, element 2j in the low nibble */
+};
+
+/* Layer parameters (host struct). */
+typedef struct kmoe_params {
+  int T;                        /* tokens, >= 0 */
+  int H;                        /* hidden size, multiple of 128 */
+  int I;                        /* expert intermediate size, multiple of 128 */
+  int E;                        /* experts, 1..1024 */
+  int k;                        /* experts per token, 1..min(E, 32) */
+  float situ_beta;              /* SiTU gate beta (Kimi-K3: 4.0) */
+  float situ_linear_beta;       /* SiTU linear beta (Kimi-K3: 25.0) */
+  float routed_scaling_factor;  /* applied in the combine (1.0 in the workloads) */
+  uint32_t flags;               /* reserved, must be 0 */
+} kmoe_params;
+
+/* Human-readable name of a status code (static string). */
+const char* kmoe_status_string(int status);
+
+/* Checks that `device` is a GB300-class GPU (compute capability 10.3) and
+ * that this library's kernels load on it.  Call once at initialisation;
+ * returns KMOE_ERR_ARCH otherwise (fail at init, never at the first layer). */
+int kmoe_check_device(int device);
+
+/* Bytes of device workspace kmoe_forward needs for these parameters (0 on
+ * invalid parameters). */
+size_t kmoe_workspace_size(const kmoe_params* p);
+
+/* Offsets (bytes from the workspace base) of the stage tensors kmoe_forward
+ * leaves in the workspace, for inspection and tests.  Host struct. */
+typedef struct kmoe_ws_layout {
+  size_t err;          /* uint32 device error word (KMOE_DEVERR_* bits) */
+  size_t topk_ids;     /* int32 [T, k] expert ids used (routed or given) */
+  size_t topk_w;       /* float [T, k] routing weights used */
+  size_t counts;       /* int32 [E] rows per expert */
+  size_t seg_start;    /* int32 [E+1] first expert-sorted row of each expert */
+  size_t tile_start;   /* int32 [E+1] first tile of each expert */
+  size_t row_of_slot;  /* int32 [T*k] expert-sorted row of slot t*k+j (-1 if masked) */
+  size_t slot_of_row;  /* int32 [R] slot t*k+j of each expert-sorted row */
+  size_t xq;           /* uint8 [R, H] E4M3 codes of x, expert-sorted */
+  size_t xsf;          /* uint8 tile-layout UE8M0 scales of xq (see kmoe_tile_sf_offset) */
+  size_t iq;           /* uint8 [R, I] E4M3 codes of SiTU(FC1), expert-sorted */
+  size_t isf;          /* uint8 tile-layout UE8M0 scales of iq */
+  size_t y;            /* float [T*k, H] per-slot FC2 outputs (slot order) */
+  int tile_rows;       /* rows per token tile (BN) chosen for these parameters */
+  int max_tiles;       /* capacity of the tile-layout scale arrays, in tiles */
+  size_t total;        /* == kmoe_workspace_size(p) */
+} kmoe_ws_layout;
+int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out /* host */);
+
+/* Routing (Kimi-K3 TopK: sigmoid scores, e_score_correction_bias used only
+ * to choose, weights gathered from the un-biased scores and renormalised).
+ * key[e] = fp32(sigmoid(logit[e])) + bias[e] (one fp32 add; the sigmoid is
+ * evaluated in double and rounded once); the k largest keys are chosen,
+ * equal keys going to the lower expert index; slot j holds the j-th largest
+ * key.  topk_w[t, j] = s_j / sum_j' s_j' (float, sums to 1).
+ *   logits [T, E] float, bias [E] float, topk_ids [T, k] int32 (out),
+ *   topk_w [T, k] float (out).  E <= 1024, k <= min(E, 32). */
+int kmoe_route(const float* logits, const float* bias, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+               cudaStream_t stream);
+
+/* Microscaling quantisation of bf16 rows, one UE8M0 scale per 32 columns.
+ * Scale byte = e + 127 with e the smallest integer such that
+ * amax <= qmax * 2^e (qmax = 448 for E4M3, 6 for E2M1), clamped to
+ * [-127, 127]; NaN is ignored by the absmax; codes are round-to-nearest-even
+ * of x * 2^-e, saturating to +-qmax; NaN elements become +0.  The scale row
+ * is cols/32 bytes, i.e. cols/128 little-endian int32 words (four scale
+ * bytes per int32).
+ *   x [rows, cols] bf16, cols a multiple of 128;
+ *   codes [rows, cols] (E4M3) or [rows, cols/2] (E2M1) uint8 (out);
+ *   scales [rows, cols/32] uint8 (out).  x and codes 16-byte aligned. */
+int kmoe_quantize_mx(const void* x_bf16, int rows, int cols, int fmt, uint8_t* codes, uint8_t* scales,
+                     cudaStream_t stream);
+
+/* Bytes of the re-laid-out weight scales (which = 0: w13, 1: w2); equal to
+ * the raw scale bytes (E*2I*H/32 and E*H*I/32). */
+size_t kmoe_prepared_scale_bytes(const kmoe_params* p, int which);
+
+/* One-time weight preparation (load time, not per forward): re-lays the
+ * raw row-major UE8M0 weight scales into the order in which the GEMMs copy
+ * them into tensor memory (per 128-row weight tile and per 128-wide K
+ * block, a 512-byte block of 32 lanes x 4 rows x 4 K-groups).  The FP4
+ * codes are used as given.
+ *   w13_sf [E, 2I, H/32], w2_sf [E, H, I/32] raw (in);
+ *   w13_sf_k, w2_sf_k (out, kmoe_prepared_scale_bytes each, 16-byte aligned). */
+int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13_sf, const uint8_t* w2_sf, uint8_t* w13_sf_k,
+                         uint8_t* w2_sf_k, cudaStream_t stream);
+
+/* The routed-expert MoE forward:
+ *   route (unless topk_ids/topk_w are given) -> MXFP8-quantise x ->
+ *   expert-sorted permutation -> FC1 (x . w13^T, gate and up) -> SiTU ->
+ *   MXFP8 requantise -> FC2 (. w2^T) -> out[t] = bf16(rsf * sum_j w_j y_j)
+ *   with slots summed in order j = 0..k-1 in fp32 (deterministic).
+ * x [T, H] bf16 (16-byte aligned); logits/bias as kmoe_route (ignored when
+ * topk_ids is given); w13/w2 codes 32-byte aligned; w13_sf_k/w2_sf_k from
+ * kmoe_prepare_weights; topk_ids [T, k] int32 and topk_w [T, k] float
+ * optional (both or neither; an id < 0 marks a masked slot that adds 0;
+ * an id >= E raises KMOE_ERR_DEVICE via kmoe_device_error and is masked);
+ * out [T, H] bf16 (16-byte aligned); workspace of kmoe_workspace_size(p)
+ * bytes, 256-byte aligned, reused by every call (not thread-safe per
+ * workspace). */
+int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
+                 const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
+                 const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace, size_t ws_bytes,
+                 cudaStream_t stream);
+
+/* Reads the device error word of `workspace` (synchronises `stream`), clears
+ * it, and returns KMOE_OK, KMOE_ERR_TIMEOUT or KMOE_ERR_DEVICE.  *word (host,
+ * may be null) receives the raw bits (1: a bounded wait timed out, 2: an
+ * expert id >= E was seen).  kmoe_forward clears the word when it starts, so
+ * it reports the most recent forward on that workspace. */
+int kmoe_device_error(void* workspace, uint32_t* word, cudaStream_t stream);
+
+/* Byte offset, inside a tile-layout scale array (xsf/isf of the workspace),
+ * of the scale of row `local_row` of token tile `tile` for 32-group `g`
+ * (K index 32g..32g+31), given the tile size, the K width in elements and the
+ * tile capacity of the array.  Host helper for inspection. */
+size_t kmoe_tile_sf_offset(int tile, int local_row, int g, int tile_rows, int K, int max_tiles);
+
+/* Self-test of the bounded device wait: launches one block that waits on a
+ * barrier nobody arrives at, for at most `budget_us` microseconds, and
+ * reports the outcome in workspace's error word (read it with
+ * kmoe_device_error, which must then return KMOE_ERR_TIMEOUT). */
+int kmoe_selftest_wait_timeout(void* workspace, int budget_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KMOE_H_ */

@@ -1,0 +1,233 @@
+"""Python binding of libkmoe: the Kimi-K3 routed-expert MoE forward
+(MXFP8 activations x MXFP4 weights, SiTU) for GB300 (sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+The functions carry the C entry points' names (include/kmoe.h); torch is used
+for device memory and the current stream.  Importing this package loads the
+in-tree libkmoe.so and raises if it is missing (build it with
+`python -m mxfp8_mxfp4_moe_gb300.build` or __graft_entry__.build()).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkmoe.so")
+
+KMOE_OK = 0
+STATUS = {0: "KMOE_OK", 1: "KMOE_ERR_ARG", 2: "KMOE_ERR_SHAPE", 3: "KMOE_ERR_ALIGN", 4: "KMOE_ERR_ARCH",
+          5: "KMOE_ERR_WORKSPACE", 6: "KMOE_ERR_CUDA", 7: "KMOE_ERR_TIMEOUT", 8: "KMOE_ERR_DEVICE"}
+KMOE_MXFP8_E4M3 = 0
+KMOE_MXFP4_E2M1 = 1
+
+EXPORTS = ("kmoe_status_string", "kmoe_check_device", "kmoe_workspace_size", "kmoe_workspace_layout",
+           "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_scale_bytes", "kmoe_prepare_weights",
+           "kmoe_forward", "kmoe_device_error", "kmoe_tile_sf_offset", "kmoe_selftest_wait_timeout")
+
+
+class kmoe_params(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
+                ("k", ctypes.c_int), ("situ_beta", ctypes.c_float), ("situ_linear_beta", ctypes.c_float),
+                ("routed_scaling_factor", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class kmoe_ws_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("err", "topk_ids", "topk_w", "counts", "seg_start", "tile_start",
+                                               "row_of_slot", "slot_of_row", "xq", "xsf", "iq", "isf", "y")] + \
+               [("tile_rows", ctypes.c_int), ("max_tiles", ctypes.c_int), ("total", ctypes.c_size_t)]
+
+
+class KmoeError(RuntimeError):
+    def __init__(self, fn, status, lib=None):
+        msg = STATUS.get(status, str(status))
+        if lib is not None:
+            msg += ": " + lib.kmoe_status_string(status).decode()
+        super().__init__(f"{fn} failed with {msg}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError(f"libkmoe.so not built at {path}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, S, I, V = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+    pp = ctypes.POINTER(kmoe_params)
+    lib.kmoe_status_string.restype = ctypes.c_char_p
+    lib.kmoe_status_string.argtypes = [I]
+    lib.kmoe_check_device.argtypes = [I]
+    lib.kmoe_workspace_size.restype = S
+    lib.kmoe_workspace_size.argtypes = [pp]
+    lib.kmoe_workspace_layout.argtypes = [pp, ctypes.POINTER(kmoe_ws_layout)]
+    lib.kmoe_route.argtypes = [P, P, I, I, I, P, P, V]
+    lib.kmoe_quantize_mx.argtypes = [P, I, I, I, P, P, V]
+    lib.kmoe_prepared_scale_bytes.restype = S
+    lib.kmoe_prepared_scale_bytes.argtypes = [pp, I]
+    lib.kmoe_prepare_weights.argtypes = [pp, P, P, P, P, V]
+    lib.kmoe_forward.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, S, V]
+    lib.kmoe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), V]
+    lib.kmoe_tile_sf_offset.restype = S
+    lib.kmoe_tile_sf_offset.argtypes = [I, I, I, I, I, I]
+    lib.kmoe_selftest_wait_timeout.argtypes = [P, I, V]
+    for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
+              "kmoe_prepare_weights", "kmoe_forward", "kmoe_device_error", "kmoe_selftest_wait_timeout"):
+        getattr(lib, n).restype = ctypes.c_int
+    return lib
+
+
+_lib = load_library()
+
+
+def lib():
+    return _lib
+
+
+def _check(fn, st):
+    if st != KMOE_OK:
+        raise KmoeError(fn, st, _lib)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (strided input is rejected, not copied)")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def make_params(T, H, I, E, k, situ_beta=4.0, situ_linear_beta=25.0, routed_scaling_factor=1.0):
+    return kmoe_params(T, H, I, E, k, situ_beta, situ_linear_beta, routed_scaling_factor, 0)
+
+
+def kmoe_status_string(status: int) -> str:
+    return _lib.kmoe_status_string(status).decode()
+
+
+def kmoe_check_device(device: int = 0) -> int:
+    return _lib.kmoe_check_device(device)
+
+
+def kmoe_workspace_size(p: kmoe_params) -> int:
+    return _lib.kmoe_workspace_size(ctypes.byref(p))
+
+
+def kmoe_workspace_layout(p: kmoe_params) -> kmoe_ws_layout:
+    out = kmoe_ws_layout()
+    _check("kmoe_workspace_layout", _lib.kmoe_workspace_layout(ctypes.byref(p), ctypes.byref(out)))
+    return out
+
+
+def kmoe_route(logits, bias, k, topk_ids=None, topk_w=None, stream=None):
+    _dev(logits, "logits", torch.float32)
+    _dev(bias, "bias", torch.float32)
+    T, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check("kmoe_route", _lib.kmoe_route(_ptr(logits), _ptr(bias), T, E, k, _ptr(topk_ids), _ptr(topk_w),
+                                         _stream(stream)))
+    return topk_ids, topk_w
+
+
+def kmoe_quantize_mx(x, fmt=KMOE_MXFP8_E4M3, codes=None, scales=None, stream=None):
+    _dev(x, "x", torch.bfloat16)
+    rows, cols = x.shape
+    if codes is None:
+        codes = torch.empty((rows, cols if fmt == KMOE_MXFP8_E4M3 else cols // 2), dtype=torch.uint8,
+                            device=x.device)
+    if scales is None:
+        scales = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+    _check("kmoe_quantize_mx", _lib.kmoe_quantize_mx(_ptr(x), rows, cols, fmt, _ptr(codes), _ptr(scales),
+                                                     _stream(stream)))
+    return codes, scales
+
+
+def kmoe_prepare_weights(p, w13_sf, w2_sf, stream=None):
+    _dev(w13_sf, "w13_sf", torch.uint8)
+    _dev(w2_sf, "w2_sf", torch.uint8)
+    n13 = _lib.kmoe_prepared_scale_bytes(ctypes.byref(p), 0)
+    n2 = _lib.kmoe_prepared_scale_bytes(ctypes.byref(p), 1)
+    if n13 == 0 or w13_sf.numel() != n13 or w2_sf.numel() != n2:
+        raise ValueError("weight scale sizes do not match the parameters")
+    a = torch.empty(n13, dtype=torch.uint8, device=w13_sf.device)
+    b = torch.empty(n2, dtype=torch.uint8, device=w13_sf.device)
+    _check("kmoe_prepare_weights", _lib.kmoe_prepare_weights(ctypes.byref(p), _ptr(w13_sf), _ptr(w2_sf), _ptr(a),
+                                                             _ptr(b), _stream(stream)))
+    return a, b
+
+
+def kmoe_forward(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, topk_w=None, out=None,
+                 workspace=None, stream=None):
+    _dev(x, "x", torch.bfloat16)
+    for n, t in (("w13", w13), ("w13_sf_k", w13_sf_k), ("w2", w2), ("w2_sf_k", w2_sf_k)):
+        _dev(t, n, torch.uint8)
+    if topk_ids is None:
+        _dev(logits, "logits", torch.float32)
+        _dev(bias, "bias", torch.float32)
+    else:
+        _dev(topk_ids, "topk_ids", torch.int32)
+        _dev(topk_w, "topk_w", torch.float32)
+    if out is None:
+        out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(kmoe_workspace_size(p), dtype=torch.uint8, device=x.device)
+    _check("kmoe_forward", _lib.kmoe_forward(
+        ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(w13_sf_k), _ptr(w2), _ptr(w2_sf_k),
+        _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out, workspace
+
+
+def kmoe_device_error(workspace, stream=None):
+    word = ctypes.c_uint32(0)
+    st = _lib.kmoe_device_error(_ptr(workspace), ctypes.byref(word), _stream(stream))
+    return st, word.value
+
+
+def kmoe_tile_sf_offset(tile, local_row, g, tile_rows, K, max_tiles):
+    return _lib.kmoe_tile_sf_offset(tile, local_row, g, tile_rows, K, max_tiles)
+
+
+def kmoe_selftest_wait_timeout(workspace, budget_us, stream=None):
+    _check("kmoe_selftest_wait_timeout",
+           _lib.kmoe_selftest_wait_timeout(_ptr(workspace), budget_us, _stream(stream)))
+
+
+def stage_views(p, workspace):
+    """Views of the stage tensors kmoe_forward leaves in the workspace."""
+    L = kmoe_workspace_layout(p)
+    R = p.T * p.k
+
+    def v(off, n, dtype):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return workspace[off:off + nbytes].view(dtype)
+
+    return {
+        "layout": L,
+        "topk_ids": v(L.topk_ids, R, torch.int32).view(p.T, p.k),
+        "topk_w": v(L.topk_w, R, torch.float32).view(p.T, p.k),
+        "counts": v(L.counts, p.E, torch.int32),
+        "seg_start": v(L.seg_start, p.E + 1, torch.int32),
+        "tile_start": v(L.tile_start, p.E + 1, torch.int32),
+        "row_of_slot": v(L.row_of_slot, R, torch.int32),
+        "slot_of_row": v(L.slot_of_row, R, torch.int32),
+        "xq": v(L.xq, R * p.H, torch.uint8).view(R, p.H),
+        "iq": v(L.iq, R * p.I, torch.uint8).view(R, p.I),
+        "xsf": workspace[L.xsf:L.xsf + (p.H // 128) * L.max_tiles * ((L.tile_rows + 127) // 128) * 512],
+        "isf": workspace[L.isf:L.isf + (p.I // 128) * L.max_tiles * ((L.tile_rows + 127) // 128) * 512],
+        "y": v(L.y, R * p.H, torch.float32).view(R, p.H),
+    }

@@ -1,0 +1,289 @@
+// C-ABI entry points of libkmoe (declared and documented in include/kmoe.h):
+// argument checks, the workspace layout, TMA tensor-map construction and the
+// stream-ordered launch sequence of the forward.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace kmoe {
+cudaError_t launch_route(const float*, const float*, int, int, int, int32_t*, float*, cudaStream_t);
+cudaError_t launch_permute(const int32_t*, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
+                           uint32_t*, cudaStream_t);
+cudaError_t launch_quant_rows(const void*, int, int, int, uint8_t*, uint8_t*, cudaStream_t);
+cudaError_t launch_quant_scatter(const void*, int, int, int, int, int, int, int, const int32_t*, const int32_t*,
+                                 const int32_t*, const int32_t*, const int32_t*, int32_t*, int32_t*, uint8_t*,
+                                 uint8_t*, cudaStream_t);
+cudaError_t launch_combine(const float*, const int32_t*, const float*, int, int, int, int, float, void*,
+                           cudaStream_t);
+cudaError_t launch_prep_wsf(const uint8_t*, uint8_t*, int, int, int, int, int, int, int, cudaStream_t);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t budget_ns, cudaStream_t st);
+__global__ void kmoe_probe_kernel();
+}  // namespace kmoe
+
+using namespace kmoe;
+
+namespace {
+
+constexpr unsigned long long kWaitBudgetNs = 2000000000ull;  // 2 s per device-side wait
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D tensor map over [rows, cols] elements with row stride `stride_bytes`.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+              uint64_t stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[2] = {cols, rows};
+  cuuint64_t gstr[1] = {stride_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_params(const kmoe_params* p) {
+  if (!p) return KMOE_ERR_ARG;
+  if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->k <= 0 || p->flags != 0) return KMOE_ERR_ARG;
+  if (p->E > kMaxE || p->k > p->E || p->k > kMaxK) return KMOE_ERR_ARG;
+  if (p->H % 128 != 0 || p->I % 128 != 0) return KMOE_ERR_SHAPE;
+  // row indices of the weight tensor maps stay within int range
+  if (static_cast<long long>(p->E) * 2 * p->I >= (1LL << 31) || static_cast<long long>(p->E) * p->H >= (1LL << 31))
+    return KMOE_ERR_SHAPE;
+  if (static_cast<long long>(p->T) * p->k >= (1LL << 31)) return KMOE_ERR_SHAPE;
+  return KMOE_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+#define KMOE_CK(call)                           \
+  do {                                          \
+    if ((call) != cudaSuccess) return KMOE_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* kmoe_status_string(int s) {
+  switch (s) {
+    case KMOE_OK: return "ok";
+    case KMOE_ERR_ARG: return "invalid argument";
+    case KMOE_ERR_SHAPE: return "unsupported shape (H and I must be multiples of 128; FC1 rows = 2 x FC2 K)";
+    case KMOE_ERR_ALIGN: return "misaligned pointer";
+    case KMOE_ERR_ARCH: return "device is not compute capability 10.3 (GB300) or the kernels do not load";
+    case KMOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case KMOE_ERR_CUDA: return "CUDA call failed";
+    case KMOE_ERR_TIMEOUT: return "a device-side wait timed out";
+    case KMOE_ERR_DEVICE: return "device-side error (expert id out of range)";
+    default: return "unknown status";
+  }
+}
+
+int kmoe_check_device(int device) {
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return KMOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return KMOE_ERR_ARCH;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return KMOE_ERR_CUDA;
+  if (cur != device && cudaSetDevice(device) != cudaSuccess) return KMOE_ERR_CUDA;
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(kmoe_probe_kernel));
+  if (cur != device) cudaSetDevice(cur);
+  if (e != cudaSuccess) return KMOE_ERR_ARCH;
+  if (!encode_fn()) return KMOE_ERR_CUDA;
+  return KMOE_OK;
+}
+
+size_t kmoe_workspace_size(const kmoe_params* p) {
+  if (check_params(p) != KMOE_OK) return 0;
+  Layout L;
+  if (!make_layout(*p, L)) return 0;
+  return L.total;
+}
+
+int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out) {
+  int st = check_params(p);
+  if (st != KMOE_OK) return st;
+  if (!out) return KMOE_ERR_ARG;
+  Layout L;
+  if (!make_layout(*p, L)) return KMOE_ERR_ARG;
+  out->err = L.err;
+  out->topk_ids = L.topk_ids;
+  out->topk_w = L.topk_w;
+  out->counts = L.counts;
+  out->seg_start = L.seg_start;
+  out->tile_start = L.tile_start;
+  out->row_of_slot = L.row_of_slot;
+  out->slot_of_row = L.slot_of_row;
+  out->xq = L.xq;
+  out->xsf = L.xsf;
+  out->iq = L.iq;
+  out->isf = L.isf;
+  out->y = L.y;
+  out->tile_rows = L.BN;
+  out->max_tiles = L.max_tiles;
+  out->total = L.total;
+  return KMOE_OK;
+}
+
+size_t kmoe_tile_sf_offset(int tile, int local_row, int g, int tile_rows, int K, int max_tiles) {
+  (void)K;
+  return tile_sf_offset(tile, local_row, g, (tile_rows + 127) / 128, max_tiles);
+}
+
+int kmoe_route(const float* logits, const float* bias, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+               cudaStream_t stream) {
+  if (T < 0 || E <= 0 || E > kMaxE || k <= 0 || k > E || k > kMaxK) return KMOE_ERR_ARG;
+  if (T > 0 && (!logits || !bias || !topk_ids || !topk_w)) return KMOE_ERR_ARG;
+  KMOE_CK(launch_route(logits, bias, T, E, k, topk_ids, topk_w, stream));
+  return KMOE_OK;
+}
+
+int kmoe_quantize_mx(const void* x_bf16, int rows, int cols, int fmt, uint8_t* codes, uint8_t* scales,
+                     cudaStream_t stream) {
+  if (rows < 0 || cols <= 0) return KMOE_ERR_ARG;
+  if (fmt != KMOE_MXFP8_E4M3 && fmt != KMOE_MXFP4_E2M1) return KMOE_ERR_ARG;
+  if (cols % 128 != 0) return KMOE_ERR_SHAPE;
+  if (rows == 0) return KMOE_OK;
+  if (!x_bf16 || !codes || !scales) return KMOE_ERR_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(codes, 16)) return KMOE_ERR_ALIGN;
+  KMOE_CK(launch_quant_rows(x_bf16, rows, cols, fmt, codes, scales, stream));
+  return KMOE_OK;
+}
+
+size_t kmoe_prepared_scale_bytes(const kmoe_params* p, int which) {
+  if (check_params(p) != KMOE_OK) return 0;
+  if (which == 0) return static_cast<size_t>(p->E) * 2 * p->I * (p->H / 32);
+  if (which == 1) return static_cast<size_t>(p->E) * p->H * (p->I / 32);
+  return 0;
+}
+
+int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13_sf, const uint8_t* w2_sf, uint8_t* w13_sf_k,
+                         uint8_t* w2_sf_k, cudaStream_t stream) {
+  int st = check_params(p);
+  if (st != KMOE_OK) return st;
+  if (!w13_sf || !w2_sf || !w13_sf_k || !w2_sf_k) return KMOE_ERR_ARG;
+  if (!aligned(w13_sf_k, 16) || !aligned(w2_sf_k, 16)) return KMOE_ERR_ALIGN;
+  KMOE_CK(launch_prep_wsf(w13_sf, w13_sf_k, p->E, p->I / 64, p->H / 128, 2 * p->I, p->H / 32, 1, p->I, stream));
+  KMOE_CK(launch_prep_wsf(w2_sf, w2_sf_k, p->E, p->H / 128, p->I / 128, p->H, p->I / 32, 0, p->I, stream));
+  return KMOE_OK;
+}
+
+int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
+                 const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
+                 const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace, size_t ws_bytes,
+                 cudaStream_t stream) {
+  int st = check_params(p);
+  if (st != KMOE_OK) return st;
+  Layout L;
+  if (!make_layout(*p, L)) return KMOE_ERR_ARG;
+  if (!workspace || ws_bytes < L.total) return KMOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KMOE_ERR_ALIGN;
+  if (p->T == 0) return KMOE_OK;
+  const bool given = topk_ids != nullptr;
+  if ((topk_ids == nullptr) != (topk_w == nullptr)) return KMOE_ERR_ARG;
+  if (!x_bf16 || !w13 || !w13_sf_k || !w2 || !w2_sf_k || !out_bf16) return KMOE_ERR_ARG;
+  if (!given && (!logits || !bias)) return KMOE_ERR_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(out_bf16, 16) || !aligned(w13, 32) || !aligned(w2, 32) ||
+      !aligned(w13_sf_k, 16) || !aligned(w2_sf_k, 16))
+    return KMOE_ERR_ALIGN;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws + L.err);
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + L.topk_ids);
+  float* wts = reinterpret_cast<float*>(ws + L.topk_w);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* seg_start = reinterpret_cast<int32_t*>(ws + L.seg_start);
+  int32_t* tile_start = reinterpret_cast<int32_t*>(ws + L.tile_start);
+  int32_t* chunk_prefix = reinterpret_cast<int32_t*>(ws + L.chunk_prefix);
+  int32_t* rank = reinterpret_cast<int32_t*>(ws + L.rank);
+  int32_t* row_of_slot = reinterpret_cast<int32_t*>(ws + L.row_of_slot);
+  int32_t* slot_of_row = reinterpret_cast<int32_t*>(ws + L.slot_of_row);
+  uint8_t* xq = ws + L.xq;
+  uint8_t* xsf = ws + L.xsf;
+  uint8_t* iq = ws + L.iq;
+  uint8_t* isf = ws + L.isf;
+  float* y = reinterpret_cast<float*>(ws + L.y);
+  const int T = p->T, H = p->H, I = p->I, E = p->E, k = p->k, R = L.R;
+
+  // tensor maps: weights as E2M1 (unpacked to 16-byte aligned groups in smem), token rows as bytes
+  CUtensorMap mA1, mA2, mB1, mB2;
+  if (!make_map(&mA1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, static_cast<uint64_t>(E) * 2 * I, H / 2, 128,
+                64) ||
+      !make_map(&mA2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, static_cast<uint64_t>(E) * H, I / 2, 128, 128) ||
+      !make_map(&mB1, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, H, R, H, 128, 32) ||
+      !make_map(&mB2, CU_TENSOR_MAP_DATA_TYPE_UINT8, iq, I, R, I, 128, 32))
+    return KMOE_ERR_CUDA;
+
+  KMOE_CK(cudaMemsetAsync(err, 0, 16, stream));  // the error word reports this call only
+  if (given) {
+    KMOE_CK(cudaMemcpyAsync(ids, topk_ids, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
+    KMOE_CK(cudaMemcpyAsync(wts, topk_w, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
+  } else {
+    KMOE_CK(launch_route(logits, bias, T, E, k, ids, wts, stream));
+  }
+  KMOE_CK(launch_permute(ids, R, E, L.BN, rank, chunk_prefix, counts, seg_start, tile_start, err, stream));
+  KMOE_CK(launch_quant_scatter(x_bf16, T, H, k, E, L.BN, L.nch, L.max_tiles, ids, rank, chunk_prefix, seg_start,
+                               tile_start, row_of_slot, slot_of_row, xq, xsf, stream));
+  const int grid = num_sms();
+  if (grid <= 0) return KMOE_ERR_CUDA;
+  GemmArgs a1{counts, seg_start, tile_start, w13_sf_k, xsf, E, I / 64, H / 128, L.max_tiles, H, I,
+              iq, isf, p->situ_beta, p->situ_linear_beta, nullptr, slot_of_row, err, kWaitBudgetNs};
+  KMOE_CK(launch_moe_gemm(true, L.BN, mA1, mB1, a1, grid, stream));
+  GemmArgs a2{counts, seg_start, tile_start, w2_sf_k, isf, E, H / 128, I / 128, L.max_tiles, H, I,
+              nullptr, nullptr, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs};
+  KMOE_CK(launch_moe_gemm(false, L.BN, mA2, mB2, a2, grid, stream));
+  KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));
+  return KMOE_OK;
+}
+
+int kmoe_device_error(void* workspace, uint32_t* word, cudaStream_t stream) {
+  if (!workspace) return KMOE_ERR_ARG;
+  uint32_t v = 0;
+  uint32_t* dev = static_cast<uint32_t*>(workspace);  // the error word is at offset 0
+  KMOE_CK(cudaMemcpyAsync(&v, dev, 4, cudaMemcpyDeviceToHost, stream));
+  KMOE_CK(cudaStreamSynchronize(stream));
+  KMOE_CK(cudaMemsetAsync(dev, 0, 4, stream));
+  KMOE_CK(cudaStreamSynchronize(stream));
+  if (word) *word = v;
+  if (v & KMOE_DEVERR_TIMEOUT) return KMOE_ERR_TIMEOUT;
+  if (v) return KMOE_ERR_DEVICE;
+  return KMOE_OK;
+}
+
+int kmoe_selftest_wait_timeout(void* workspace, int budget_us, cudaStream_t stream) {
+  if (!workspace || budget_us <= 0 || budget_us > 1000000) return KMOE_ERR_ARG;
+  KMOE_CK(launch_wait_selftest(static_cast<uint32_t*>(workspace), static_cast<uint64_t>(budget_us) * 1000ull,
+                               stream));
+  return KMOE_OK;
+}
+
+}  // extern "C"

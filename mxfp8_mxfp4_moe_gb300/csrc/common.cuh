@@ -1,0 +1,108 @@
+// Shared definitions of the kmoe kernels: status handling, the workspace
+// layout, the token-tile scale layout and small numeric helpers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/kmoe.h"
+#include "ptx.cuh"
+
+namespace kmoe {
+
+constexpr int kRankChunk = 1024;  // slots per block in the stable rank pass
+constexpr int kMaxE = 1024;       // experts supported by the routing kernel
+constexpr int kMaxK = 32;
+
+// ---------------------------------------------------------------- tile layout
+// Scales of the B operand (token rows) are stored per token tile so that a
+// tile's scales for one 128-wide K block form whole 512-byte blocks that
+// tcgen05.cp copies into TMEM at a 4-aligned column:
+//   block (kb, tile, chunk) = 512 bytes, chunk = local_row / 128,
+//   byte j*16 + c*4 + g%4 holds row 32c + j (of the chunk) for K group g.
+__host__ __device__ __forceinline__ size_t tile_sf_offset(int tile, int local_row, int g, int nch, int max_tiles) {
+  const int kb = g >> 2;
+  const int chunk = local_row >> 7;
+  const int r = local_row & 127;
+  return ((static_cast<size_t>(kb) * max_tiles + tile) * nch + chunk) * 512 + (r & 31) * 16 + (r >> 5) * 4 +
+         (g & 3);
+}
+
+// ---------------------------------------------------------------- workspace
+struct Layout {
+  size_t err, topk_ids, topk_w, counts, seg_start, tile_start, chunk_prefix, rank, row_of_slot, slot_of_row;
+  size_t xq, xsf, iq, isf, y, total;
+  int R, BN, nch, max_tiles, nchunk;
+};
+
+// Token-tile size for a layer: small tiles when few rows reach each expert
+// (decode), large tiles when many do (prefill).
+__host__ inline int choose_tile_rows(long long R, int E) {
+  const double avg = static_cast<double>(R) / E;
+  if (avg <= 20.0) return 32;
+  if (avg <= 48.0) return 64;
+  return 224;
+}
+
+__host__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__host__ inline bool make_layout(const kmoe_params& p, Layout& L) {
+  if (p.T < 0 || p.H <= 0 || p.I <= 0 || p.E <= 0 || p.k <= 0) return false;
+  const size_t R = static_cast<size_t>(p.T) * p.k;
+  L.R = static_cast<int>(R);
+  L.BN = choose_tile_rows(static_cast<long long>(R), p.E);
+  L.nch = (L.BN + 127) / 128;
+  L.max_tiles = static_cast<int>((R + L.BN - 1) / L.BN + (R < static_cast<size_t>(p.E) ? R : p.E));
+  if (L.max_tiles < 1) L.max_tiles = 1;
+  L.nchunk = static_cast<int>((R + kRankChunk - 1) / kRankChunk);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + (bytes ? bytes : 1), 256);
+    return o;
+  };
+  L.err = take(16);
+  L.topk_ids = take(R * 4);
+  L.topk_w = take(R * 4);
+  L.counts = take(static_cast<size_t>(p.E) * 4);
+  L.seg_start = take(static_cast<size_t>(p.E + 1) * 4);
+  L.tile_start = take(static_cast<size_t>(p.E + 1) * 4);
+  L.chunk_prefix = take(static_cast<size_t>(L.nchunk) * p.E * 4);
+  L.rank = take(R * 4);
+  L.row_of_slot = take(R * 4);
+  L.slot_of_row = take(R * 4);
+  L.xq = take(R * p.H);
+  L.xsf = take(static_cast<size_t>(p.H / 128) * L.max_tiles * L.nch * 512);
+  L.iq = take(R * p.I);
+  L.isf = take(static_cast<size_t>(p.I / 128) * L.max_tiles * L.nch * 512);
+  L.y = take(R * p.H * 4);
+  L.total = off;
+  return true;
+}
+
+// ---------------------------------------------------------------- numerics
+// 2^n as a float for n in [-127, 127] (exact).
+__device__ __forceinline__ float exp2i(int n) {
+  return n >= -126 ? __int_as_float((n + 127) << 23) : __int_as_float(0x00200000);
+}
+
+// Scale exponent of the microscaling rule: smallest e with amax <= qmax*2^e,
+// clamped to [-127, 127], where qmax = 1.75 * 2^8 (E4M3) or 1.5 * 2^2 (E2M1).
+// amax must be >= 0 (NaN already dropped).  Works on the fp32 bit pattern:
+// amax = (1 + M/2^23) * 2^Ea, and the bound needs e = Ea - qexp (+1 when the
+// significand exceeds qmax's).
+template <int QEXP, uint32_t QMANT>
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = static_cast<int>((b >> 23) & 0xFF);
+  if (ef == 0) return -127;             // zero or subnormal: far below any bound
+  if (ef == 0xFF) return 127;           // inf
+  const int ea = ef - 127;
+  int e = ea - QEXP + ((b & 0x7FFFFF) > QMANT ? 1 : 0);
+  e = e < -127 ? -127 : (e > 127 ? 127 : e);
+  return e;
+}
+__device__ __forceinline__ int e4m3_scale_exp(float amax) { return mx_scale_exp<8, 0x600000u>(amax); }
+__device__ __forceinline__ int e2m1_scale_exp(float amax) { return mx_scale_exp<2, 0x400000u>(amax); }
+
+}  // namespace kmoe

@@ -1,0 +1,114 @@
+// Expert permutation: per-expert histogram, exclusive scans and a stable
+// rank of every routed slot among the slots of its expert, so that the rows
+// of each expert form one contiguous, token-ordered segment.  The grouped
+// GEMMs walk those segments in token tiles of `BN` rows.
+//
+//   pass 1 (rank_kernel, one block per 1024 slots): stable rank of each slot
+//          inside its block (warps in order, __match_any_sync inside a warp)
+//          and the block's per-expert counts.
+//   pass 2 (scan_kernel, one block): per-expert totals, prefix over blocks,
+//          segment starts and tile starts (prefix of ceil(count/BN)).
+// The final row of slot s is seg_start[e] + chunk_prefix[block][e] + rank[s];
+// it is computed where the row is written (the quantise-scatter kernel).
+#include "common.cuh"
+
+namespace kmoe {
+
+__global__ void __launch_bounds__(kRankChunk) rank_kernel(const int32_t* __restrict__ ids, int R, int E,
+                                                          int32_t* __restrict__ rank,
+                                                          int32_t* __restrict__ chunk_counts,
+                                                          uint32_t* __restrict__ err) {
+  extern __shared__ int cnt[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int s = blockIdx.x * kRankChunk + threadIdx.x;
+  int id = s < R ? ids[s] : -1;
+  if (id >= E) {
+    atomicOr(err, 2u);  // KMOE_DEVERR_BOUNDS: an expert id out of range (treated as masked)
+    id = -1;
+  }
+  const bool valid = id >= 0;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? id : -1);
+  const unsigned lower = peers & ((1u << lane) - 1u);
+  const int nwarps = blockDim.x >> 5;
+  int my = -1;
+  for (int w = 0; w < nwarps; ++w) {
+    int base = 0;
+    if (warp == w && valid) base = cnt[id];
+    __syncwarp();
+    if (warp == w && valid) {
+      my = base + __popc(lower);
+      if (lower == 0) cnt[id] = base + __popc(peers);
+    }
+    __syncthreads();
+  }
+  if (s < R) rank[s] = my;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+// Single block.  chunk_counts [nchunk][E] becomes its exclusive prefix over
+// chunks; counts/seg_start/tile_start are written.
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ chunk_counts, int nchunk, int E, int BN,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ seg_start,
+                                                    int32_t* __restrict__ tile_start) {
+  __shared__ int s_rows[1024];
+  __shared__ int s_tiles[1024];
+  const int per = (E + blockDim.x - 1) / blockDim.x;  // experts per thread (contiguous)
+  const int e0 = threadIdx.x * per;
+  int rows = 0, tiles = 0;
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    int run = 0;
+    for (int c = 0; c < nchunk; ++c) {
+      int32_t* p = chunk_counts + static_cast<size_t>(c) * E + e;
+      const int v = *p;
+      *p = run;
+      run += v;
+    }
+    counts[e] = run;
+    rows += run;
+    tiles += (run + BN - 1) / BN;
+  }
+  s_rows[threadIdx.x] = rows;
+  s_tiles[threadIdx.x] = tiles;
+  __syncthreads();
+  // inclusive Hillis-Steele scan over threads
+  for (int off = 1; off < blockDim.x; off <<= 1) {
+    int vr = threadIdx.x >= off ? s_rows[threadIdx.x - off] : 0;
+    int vt = threadIdx.x >= off ? s_tiles[threadIdx.x - off] : 0;
+    __syncthreads();
+    s_rows[threadIdx.x] += vr;
+    s_tiles[threadIdx.x] += vt;
+    __syncthreads();
+  }
+  int r = threadIdx.x > 0 ? s_rows[threadIdx.x - 1] : 0;
+  int t = threadIdx.x > 0 ? s_tiles[threadIdx.x - 1] : 0;
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    seg_start[e] = r;
+    tile_start[e] = t;
+    const int c = counts[e];
+    r += c;
+    t += (c + BN - 1) / BN;
+  }
+  if (threadIdx.x == blockDim.x - 1) {
+    seg_start[E] = s_rows[blockDim.x - 1];
+    tile_start[E] = s_tiles[blockDim.x - 1];
+  }
+}
+
+cudaError_t launch_permute(const int32_t* ids, int R, int E, int BN, int32_t* rank, int32_t* chunk_prefix,
+                           int32_t* counts, int32_t* seg_start, int32_t* tile_start, uint32_t* err,
+                           cudaStream_t st) {
+  const int nchunk = (R + kRankChunk - 1) / kRankChunk;
+  if (nchunk > 0) {
+    rank_kernel<<<nchunk, kRankChunk, E * sizeof(int), st>>>(ids, R, E, rank, chunk_prefix, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_prefix, nchunk, E, BN, counts, seg_start, tile_start);
+  return cudaGetLastError();
+}
+
+}  // namespace kmoe

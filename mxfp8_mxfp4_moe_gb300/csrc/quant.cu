@@ -1,0 +1,169 @@
+// Microscaling quantisation of bf16 activations (MoE path analysis page,
+// SM100 pre-dispatch: per-32 absmax -> UE8M0 scale -> FP8 E4M3 codes; the
+// SM120 page's NaN/Inf record: saturating-finite codes, never the 0xFF
+// scale).  One thread per 32-element group: four 16-byte loads, an absmax,
+// the exact power-of-two scale, and the hardware's round-to-nearest-even
+// saturating conversion.
+//
+//   quant_rows_kernel     token-major output (kmoe_quantize_mx), E4M3 or E2M1
+//   quant_scatter_kernel  forward path: codes of token t written to each of
+//                         its k expert-sorted rows, scales in the token-tile
+//                         layout the GEMM copies into TMEM
+#include <cuda_bf16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace kmoe {
+
+__device__ __forceinline__ void load_group_bf16(const __nv_bfloat16* p, float (&v)[32]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = __ldg(q + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+__device__ __forceinline__ float group_amax(const float (&v)[32]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));  // fmaxf drops NaN
+  return a;
+}
+
+__device__ __forceinline__ uint8_t e4m3_code(float x, float inv_scale) {
+  if (isnan(x)) return 0;
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x * inv_scale, __NV_SATFINITE, __NV_E4M3));
+}
+
+// 32 E4M3 codes of a group, packed little-endian into 8 words
+__device__ __forceinline__ void e4m3_group(const float (&v)[32], float inv_scale, uint32_t (&out)[8]) {
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) word |= static_cast<uint32_t>(e4m3_code(v[4 * w + b], inv_scale)) << (8 * b);
+    out[w] = word;
+  }
+}
+
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int rows, int cols,
+                                                         int fmt, uint8_t* __restrict__ codes,
+                                                         uint8_t* __restrict__ scales) {
+  const int gpr = cols / 32;
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= static_cast<long long>(rows) * gpr) return;
+  const long long r = gid / gpr;
+  const int g = static_cast<int>(gid % gpr);
+  float v[32];
+  load_group_bf16(x + r * cols + 32 * g, v);
+  const float amax = group_amax(v);
+  if (fmt == KMOE_MXFP8_E4M3) {
+    const int e = e4m3_scale_exp(amax);
+    uint32_t out[8];
+    e4m3_group(v, exp2i(-e), out);
+    uint4* dst = reinterpret_cast<uint4*>(codes + r * cols + 32 * g);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    scales[r * gpr + g] = static_cast<uint8_t>(e + 127);
+  } else {
+    const int e = e2m1_scale_exp(amax);
+    const float inv = exp2i(-e);
+    uint32_t out[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const float xv = v[8 * w + b];
+        const uint32_t c =
+            isnan(xv) ? 0u : static_cast<uint32_t>(__nv_cvt_float_to_fp4(xv * inv, __NV_E2M1, cudaRoundNearest));
+        word |= (c & 0xFu) << (4 * b);
+      }
+      out[w] = word;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(codes + r * (cols / 2) + 16 * g);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    scales[r * gpr + g] = static_cast<uint8_t>(e + 127);
+  }
+}
+
+cudaError_t launch_quant_rows(const void* x, int rows, int cols, int fmt, uint8_t* codes, uint8_t* scales,
+                              cudaStream_t st) {
+  const long long groups = static_cast<long long>(rows) * (cols / 32);
+  if (groups == 0) return cudaSuccess;
+  const long long blocks = (groups + 255) / 256;
+  quant_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), rows,
+                                                                   cols, fmt, codes, scales);
+  return cudaGetLastError();
+}
+
+// One block per token.  Threads 0..k-1 first resolve the token's k slots to
+// expert-sorted rows and token tiles; then each thread quantises 32-element
+// groups and writes the codes and scale byte once per routed slot.
+__global__ void __launch_bounds__(256) quant_scatter_kernel(
+    const __nv_bfloat16* __restrict__ x, int H, int k, int E, int BN, int nch, int max_tiles,
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, const int32_t* __restrict__ chunk_prefix,
+    const int32_t* __restrict__ seg_start, const int32_t* __restrict__ tile_start,
+    int32_t* __restrict__ row_of_slot, int32_t* __restrict__ slot_of_row, uint8_t* __restrict__ xq,
+    uint8_t* __restrict__ xsf) {
+  __shared__ int s_row[kMaxK], s_tile[kMaxK], s_local[kMaxK];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    const int s = t * k + j;
+    const int id = ids[s];
+    int row = -1, tile = -1, local = -1;
+    if (id >= 0 && id < E) {
+      const int c = s / kRankChunk;
+      const int in_seg = chunk_prefix[static_cast<size_t>(c) * E + id] + rank[s];
+      row = seg_start[id] + in_seg;
+      tile = tile_start[id] + in_seg / BN;
+      local = in_seg % BN;
+      slot_of_row[row] = s;
+    }
+    row_of_slot[s] = row;
+    s_row[j] = row;
+    s_tile[j] = tile;
+    s_local[j] = local;
+  }
+  __syncthreads();
+  const int gpr = H / 32;
+  for (int g = threadIdx.x; g < gpr; g += blockDim.x) {
+    float v[32];
+    load_group_bf16(x + static_cast<size_t>(t) * H + 32 * g, v);
+    const int e = e4m3_scale_exp(group_amax(v));
+    uint32_t out[8];
+    e4m3_group(v, exp2i(-e), out);
+    const uint4 lo = make_uint4(out[0], out[1], out[2], out[3]);
+    const uint4 hi = make_uint4(out[4], out[5], out[6], out[7]);
+    for (int j = 0; j < k; ++j) {
+      const int row = s_row[j];
+      if (row < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(row) * H + 32 * g);
+      dst[0] = lo;
+      dst[1] = hi;
+      xsf[tile_sf_offset(s_tile[j], s_local[j], g, nch, max_tiles)] = static_cast<uint8_t>(e + 127);
+    }
+  }
+}
+
+cudaError_t launch_quant_scatter(const void* x, int T, int H, int k, int E, int BN, int nch, int max_tiles,
+                                 const int32_t* ids, const int32_t* rank, const int32_t* chunk_prefix,
+                                 const int32_t* seg_start, const int32_t* tile_start, int32_t* row_of_slot,
+                                 int32_t* slot_of_row, uint8_t* xq, uint8_t* xsf, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  quant_scatter_kernel<<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), H, k, E, BN, nch, max_tiles, ids,
+                                          rank, chunk_prefix, seg_start, tile_start, row_of_slot, slot_of_row, xq,
+                                          xsf);
+  return cudaGetLastError();
+}
+
+}  // namespace kmoe

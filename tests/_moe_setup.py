@@ -1,0 +1,119 @@
+"""Shared set-up for the GPU parity tests: seeded inputs on the device and
+oracle references on the host for a token sample.  Inputs come only from the
+`workloads` generator; expected values only from `oracle`."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads as W
+from oracle import formats as F
+from oracle import moe as O
+
+_WEIGHT_CACHE = {}
+
+
+def bf16_to_torch(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def device_weights(w: W.Workload, device="cuda"):
+    import mxfp8_mxfp4_moe_gb300 as K
+    key = (w.E, w.H, w.I, w.sf_lo, w.sf_hi)
+    if key not in _WEIGHT_CACHE:
+        _WEIGHT_CACHE.clear()
+        torch.cuda.empty_cache()
+        wts = W.gen_expert_weights_torch(w, device)
+        p = params(w)
+        w13_sf_k, w2_sf_k = K.kmoe_prepare_weights(p, wts["w13_sf"], wts["w2_sf"])
+        _WEIGHT_CACHE[key] = dict(wts, w13_sf_k=w13_sf_k, w2_sf_k=w2_sf_k)
+    return _WEIGHT_CACHE[key]
+
+
+def params(w: W.Workload, **kw):
+    import mxfp8_mxfp4_moe_gb300 as K
+    d = dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, situ_beta=w.situ_beta, situ_linear_beta=w.situ_linear_beta,
+             routed_scaling_factor=w.routed_scaling_factor)
+    d.update(kw)
+    return K.make_params(**d)
+
+
+def device_inputs(w: W.Workload, small=None, device="cuda"):
+    s = small if small is not None else W.gen_small_inputs(w)
+    return {
+        "x": bf16_to_torch(s["x"], device),
+        "logits": torch.from_numpy(s["logits"]).to(device),
+        "bias": torch.from_numpy(s["bias"]).to(device),
+    }, s
+
+
+def run_forward(w, small=None, topk_ids=None, topk_w=None, device="cuda"):
+    import mxfp8_mxfp4_moe_gb300 as K
+    wt = device_weights(w, device)
+    inp, s = device_inputs(w, small, device)
+    p = params(w)
+    out, ws = K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13"], wt["w13_sf_k"], wt["w2"],
+                             wt["w2_sf_k"], topk_ids=topk_ids, topk_w=topk_w)
+    torch.cuda.synchronize()
+    st, word = K.kmoe_device_error(ws)
+    assert st == 0, f"device error word {word:#x}"
+    return out, ws, p, s, inp
+
+
+def oracle_forward(w, s, tokens, ids=None, topk_w=None):
+    """Oracle output for `tokens`, with the weights of exactly the experts they use."""
+    if ids is None:
+        ids, topk_w, _ = O.route(s["logits"], s["bias"], w.k)
+    used = sorted(set(int(e) for e in ids[tokens].ravel() if e >= 0))
+    wts = W.gen_expert_weights_np(w, used)
+    return O.forward(w, s["x"], s["logits"], s["bias"], wts, experts_host=used, tokens=tokens, ids=ids,
+                     topk_w=topk_w, want_stages=True)
+
+
+def output_errors(gpu_bf16: torch.Tensor, ref: np.ndarray):
+    g = gpu_bf16.float().cpu().numpy().astype(np.float64)
+    diff = g - ref
+    rel = np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-300)
+    mx = np.abs(diff).max() / max(np.abs(ref).max(), 1e-300)
+    return rel, mx
+
+
+def assert_output_parity(gpu_bf16, ref, tag=""):
+    rel, mx = output_errors(gpu_bf16, ref)
+    floor = np.linalg.norm(O.bf16_round(ref) - ref) / max(np.linalg.norm(ref), 1e-300)
+    print(f"{tag} rel_fro={rel:.3e} (bf16 floor {floor:.3e}) max_abs/max|ref|={mx:.3e}")
+    assert np.all(np.isfinite(gpu_bf16.float().cpu().numpy()))
+    assert rel <= 2e-3, f"{tag} relative Frobenius error {rel:.3e} > 2e-3"
+    assert mx <= 1e-2, f"{tag} max abs error {mx:.3e} x max|ref| > 1e-2"
+
+
+def tile_sf_offsets(tile, local, g, BN, max_tiles):
+    """Byte offsets in a token-tile scale array (layout plumbing, see include/kmoe.h)."""
+    nch = (BN + 127) // 128
+    kb = g // 4
+    chunk = local // 128
+    r = local % 128
+    return ((kb * max_tiles + tile) * nch + chunk) * 512 + (r % 32) * 16 + (r // 32) * 4 + (g % 4)
+
+
+def gather_row_scales(sf_bytes: np.ndarray, views_np, rows: np.ndarray, K: int):
+    """Scales [len(rows), K/32] of expert-sorted rows from a token-tile scale array."""
+    L = views_np["layout"]
+    seg = views_np["seg_start"]
+    ts = views_np["tile_start"]
+    e = np.searchsorted(seg, rows, side="right") - 1
+    # skip empty experts sharing a start: searchsorted(side=right)-1 gives the last expert starting <= row,
+    # which is the non-empty one containing it
+    local = rows - seg[e]
+    tile = ts[e] + local // L.tile_rows
+    lr = local % L.tile_rows
+    g = np.arange(K // 32)
+    off = tile_sf_offsets(tile[:, None], lr[:, None], g[None, :], L.tile_rows, L.max_tiles)
+    return sf_bytes[off]
+
+
+def stage_numpy(p, ws):
+    import mxfp8_mxfp4_moe_gb300 as K
+    v = K.stage_views(p, ws)
+    out = {k: (t.cpu().numpy() if isinstance(t, torch.Tensor) else t) for k, t in v.items()}
+    return out

@@ -1,0 +1,82 @@
+"""CPU checks of the C ABI library: it loads, exports every entry point the
+header declares, and rejects bad arguments on the host before touching a GPU.
+Also: the workload generator gives identical bytes in numpy and torch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def K():
+    import mxfp8_mxfp4_moe_gb300 as K
+    return K
+
+
+def test_library_exports_every_declared_symbol(K):
+    hdr = open(os.path.join(ROOT, "include", "kmoe.h")).read()
+    declared = set(re.findall(r"^\s*(?:const char\*|int|size_t)\s+(kmoe_\w+)\s*\(", hdr, re.M))
+    assert {"kmoe_route", "kmoe_quantize_mx", "kmoe_forward"} <= declared
+    lib = ctypes.CDLL(K.LIB_PATH)
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert set(K.EXPORTS) == declared
+
+
+def test_status_strings_and_workspace(K):
+    for s in range(9):
+        assert K.kmoe_status_string(s)
+    p = K.make_params(8192, 7168, 3584, 896, 16)
+    L = K.kmoe_workspace_layout(p)
+    assert L.tile_rows == 224 and L.total == K.kmoe_workspace_size(p)
+    offs = [L.err, L.topk_ids, L.topk_w, L.counts, L.seg_start, L.tile_start, L.row_of_slot, L.slot_of_row,
+            L.xq, L.xsf, L.iq, L.isf, L.y]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert L.y + 8192 * 16 * 7168 * 4 <= L.total
+    assert K.kmoe_workspace_layout(K.make_params(16, 7168, 3584, 896, 16)).tile_rows == 32
+    assert K.kmoe_workspace_layout(K.make_params(128, 7168, 3584, 64, 16)).tile_rows == 64
+
+
+def test_host_side_argument_errors(K):
+    lib = K.lib()
+    bad = [K.make_params(16, 100, 128, 8, 2),      # H not a multiple of 128
+           K.make_params(16, 128, 96, 8, 2),       # I not a multiple of 128
+           K.make_params(16, 128, 128, 8, 9),      # k > E
+           K.make_params(-1, 128, 128, 8, 2)]
+    for p in bad:
+        assert K.kmoe_workspace_size(p) == 0
+        st = lib.kmoe_forward(ctypes.byref(p), None, None, None, None, None, None, None, None, None, None, None, 0,
+                              None)
+        assert st in (1, 2)
+    assert lib.kmoe_route(None, None, 4, 8, 9, None, None, None) == 1
+    assert lib.kmoe_quantize_mx(None, 4, 100, 0, None, None, None) == 2
+    assert lib.kmoe_quantize_mx(None, 4, 128, 7, None, None, None) == 1
+    p = K.make_params(16, 128, 128, 8, 2)
+    n = K.kmoe_workspace_size(p)
+    # workspace too small / misaligned pointers are rejected before any CUDA call
+    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 32, 16, 32, 16, None, None, 16, 256, n - 1, None) == 5
+    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 32, 16, 32, 16, None, None, 16, 258, n, None) == 3
+    assert lib.kmoe_forward(ctypes.byref(p), 8, 16, 16, 32, 16, 32, 16, None, None, 16, 256, n, None) == 3
+    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 16, 16, 32, 16, None, None, 16, 256, n, None) == 3
+    assert lib.kmoe_tile_sf_offset(1, 33, 5, 32, 128, 10) == ((1 * 10 + 1) * 1 + 0) * 512 + 1 * 16 + 1 * 4 + 1
+
+
+def test_weight_generator_numpy_equals_torch():
+    w = W.WORKLOADS["tiny"]
+    a = W.gen_expert_weights_np(w, range(w.E))
+    b = W.gen_expert_weights_torch(w, "cpu", chunk_bytes=4096)
+    for k in a:
+        assert np.array_equal(a[k], b[k].numpy()), k
+    big = W.WORKLOADS["decode"]
+    sub = W.gen_expert_weights_np(big, [5])
+    # the counter stream is position-addressed: expert 5 alone equals its slice of a longer draw
+    per = 2 * big.I * big.H // 32
+    words = W._scales_np(W.S_W13SF, 4 * per, 2 * per, big.sf_lo, big.sf_hi, W.SEED)
+    assert np.array_equal(sub["w13_sf"][0].ravel(), words[per:])

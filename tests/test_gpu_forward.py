@@ -1,0 +1,149 @@
+"""GPU parity of the whole forward (kmoe_forward through the C ABI) against
+the float64 oracle: stage tensors (routing, MXFP8 codes and scales, expert
+permutation) bit-exact, intermediate codes by agreement rate, outputs within
+rel. Frobenius 2e-3 and max-abs 1e-2 x max|ref|.  Full-size workloads are
+checked on sampled tokens (all their routing/quantisation on every token);
+plus determinism, CUDA-graph replay, masked slots and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import formats as F
+from oracle import moe as O
+from tests._moe_setup import (assert_output_parity, device_inputs, device_weights, gather_row_scales,
+                              oracle_forward, params, run_forward, stage_numpy)
+
+pytestmark = pytest.mark.gpu
+
+TINY_UNSAT = W.WORKLOADS["tiny"].with_(name="tiny_unsaturated", sf_lo=117, sf_hi=121)
+
+
+@pytest.fixture(scope="module")
+def K():
+    import mxfp8_mxfp4_moe_gb300 as K
+    assert K.kmoe_check_device(0) == 0
+    return K
+
+
+def _check_stages(w, p, ws, s, ref, tokens):
+    st = stage_numpy(p, ws)
+    ids_ref, w_ref, _ = O.route(s["logits"], s["bias"], w.k)
+    assert np.array_equal(st["topk_ids"], ids_ref)
+    assert np.allclose(st["topk_w"], w_ref, rtol=1e-6)
+    # permutation: each slot owns exactly one row, rows of an expert are contiguous and token-ordered
+    ros = st["row_of_slot"]
+    R = w.T * w.k
+    assert sorted(ros.tolist()) == list(range(R))
+    assert np.array_equal(st["slot_of_row"][ros], np.arange(R))
+    exp_of_row = np.empty(R, np.int64)
+    exp_of_row[ros] = ids_ref.ravel()
+    assert np.all(np.diff(exp_of_row) >= 0)
+    counts = np.bincount(ids_ref.ravel(), minlength=w.E)
+    assert np.array_equal(st["counts"], counts)
+    # MXFP8 codes and scales of x, bit-exact on every token (tile layout for the scales)
+    xq_ref, xs_ref = F.quantize_mx(W.bf16_bits_to_f64(s["x"]), "e4m3")
+    slots = np.arange(R)
+    rows = ros[slots]
+    assert np.array_equal(st["xq"][rows], xq_ref[slots // w.k])
+    got_sf = gather_row_scales(st["xsf"], st, rows, w.H)
+    assert np.array_equal(got_sf, xs_ref[slots // w.k])
+    # intermediate codes of the sampled tokens: agreement rate (fp32 vs double SiTU may cross midpoints)
+    tsl = np.array([t * w.k + j for t in tokens for j in range(w.k)])
+    iq_gpu = st["iq"][ros[tsl]]
+    iq_ref = ref["inter_q"].reshape(-1, w.I)
+    same = (iq_gpu == iq_ref) | (((iq_gpu | iq_ref) & 0x7F) == 0)
+    rate = same.mean()
+    isf_gpu = gather_row_scales(st["isf"], st, ros[tsl], w.I)
+    sf_rate = (isf_gpu == ref["inter_s"].reshape(-1, w.I // 32)).mean()
+    print(f"{w.name}: intermediate code agreement {rate:.6f}, scale agreement {sf_rate:.6f}")
+    assert rate >= 0.999 and sf_rate >= 0.999
+    return st
+
+
+@pytest.mark.parametrize("wl", [W.WORKLOADS["tiny"], TINY_UNSAT], ids=["tiny", "tiny_unsaturated"])
+def test_forward_tiny_full(K, wl):
+    out, ws, p, s, _ = run_forward(wl)
+    tokens = np.arange(wl.T)
+    ref = oracle_forward(wl, s, tokens)
+    _check_stages(wl, p, ws, s, ref, tokens)
+    assert_output_parity(out, ref["out"], wl.name)
+
+
+@pytest.mark.parametrize("name,sample", [("reduced", 6), ("decode", 3), ("prefill", 2), ("skewed", 2)])
+def test_forward_full_size_sampled(K, name, sample):
+    w = W.WORKLOADS[name]
+    out, ws, p, s, _ = run_forward(w)
+    rng = np.random.default_rng(123)
+    tokens = np.sort(rng.choice(w.T, size=sample, replace=False))
+    ref = oracle_forward(w, s, tokens)
+    _check_stages(w, p, ws, s, ref, tokens)
+    assert_output_parity(out[torch.from_numpy(tokens).cuda()], ref["out"], name)
+    o = out.float()
+    assert torch.isfinite(o).all()
+
+
+def test_determinism_and_graph_replay(K):
+    for name in ("tiny", "reduced"):
+        w = W.WORKLOADS[name]
+        wt = device_weights(w)
+        inp, s = device_inputs(w)
+        p = params(w)
+        ws = torch.empty(K.kmoe_workspace_size(p), dtype=torch.uint8, device="cuda")
+        outs = []
+        for _ in range(3):
+            o = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+            K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13"], wt["w13_sf_k"], wt["w2"],
+                           wt["w2_sf_k"], out=o, workspace=ws)
+            outs.append(o)
+        torch.cuda.synchronize()
+        for o in outs[1:]:
+            assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+        # CUDA graph: capture once, replay twice, bitwise equal to eager
+        g_out = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13"], wt["w13_sf_k"], wt["w2"],
+                               wt["w2_sf_k"], out=g_out, workspace=ws, stream=stream)
+        for _ in range(2):
+            g_out.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(g_out.view(torch.int16), outs[0].view(torch.int16))
+        st, word = K.kmoe_device_error(ws)
+        assert st == 0
+
+
+def test_given_routing_masked_slots_and_hot_expert(K):
+    w = W.WORKLOADS["tiny"].with_(T=37)     # ragged: 37 tokens
+    s = W.gen_small_inputs(w)
+    ids, wts, _ = O.route(s["logits"], s["bias"], w.k)
+    ids = ids.copy()
+    ids[::3, 1] = -1                          # masked slots
+    ids[5:30, 0] = 6                          # one hot expert: > 32 rows (several token tiles)
+    wts = wts.astype(np.float32)
+    out, ws, p, _, _ = run_forward(w, small=s, topk_ids=torch.from_numpy(ids).cuda(),
+                                   topk_w=torch.from_numpy(wts).cuda())
+    ref = O.forward(w, s["x"], s["logits"], s["bias"], W.gen_expert_weights_np(w, range(w.E)), ids=ids,
+                    topk_w=wts.astype(np.float64))
+    assert_output_parity(out, ref["out"], "masked")
+
+
+def test_single_token_and_out_of_range_id(K):
+    w = W.WORKLOADS["tiny"].with_(T=1)
+    out, ws, p, s, _ = run_forward(w)
+    ref = oracle_forward(w, s, np.arange(1))
+    assert_output_parity(out, ref["out"], "T=1")
+    # an expert id >= E is reported as a device error and treated as masked
+    ids = torch.tensor([[1, 99]], dtype=torch.int32, device="cuda")
+    wts = torch.tensor([[0.5, 0.5]], dtype=torch.float32, device="cuda")
+    wt = device_weights(w)
+    inp, _ = device_inputs(w, s)
+    o, ws = K.kmoe_forward(p, inp["x"], None, None, wt["w13"], wt["w13_sf_k"], wt["w2"], wt["w2_sf_k"],
+                           topk_ids=ids, topk_w=wts)
+    st, word = K.kmoe_device_error(ws)
+    assert st == 8 and (word & 2)
+    assert torch.isfinite(o.float()).all()

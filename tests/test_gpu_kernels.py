@@ -1,0 +1,112 @@
+"""GPU parity of the routing and quantisation kernels against the oracle,
+through the C ABI: bit-exact ids, codes and scales; weights to fp32
+rounding; edge cases; the bounded-wait self-test and device error reporting."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import formats as F
+from oracle import moe as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def K():
+    import mxfp8_mxfp4_moe_gb300 as K
+    assert K.kmoe_check_device(0) == 0
+    return K
+
+
+def test_check_device(K):
+    assert K.kmoe_check_device(0) == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "reduced", "decode", "prefill", "skewed"])
+def test_route_bit_exact(K, name):
+    w = W.WORKLOADS[name]
+    s = W.gen_small_inputs(w)
+    ids_ref, w_ref, _ = O.route(s["logits"], s["bias"], w.k)
+    ids, wts = K.kmoe_route(torch.from_numpy(s["logits"]).cuda(), torch.from_numpy(s["bias"]).cuda(), w.k)
+    ids = ids.cpu().numpy()
+    wts = wts.cpu().numpy().astype(np.float64)
+    assert np.array_equal(ids, ids_ref), f"{(ids != ids_ref).sum()} routing ids differ"
+    assert np.allclose(wts, w_ref, rtol=1e-6, atol=0)
+    assert np.allclose(wts.sum(1), 1.0, atol=1e-6)
+
+
+def test_route_ties_and_k_equals_e(K):
+    T, E = 5, 64
+    logits = np.zeros((T, E), np.float32)
+    logits[1, [3, 40, 41]] = 2.0                  # exact ties
+    logits[2] = np.linspace(-3, 3, E, dtype=np.float32)
+    bias = np.zeros(E, np.float32)
+    bias[7] = 0.5
+    for k in (1, 3, 16, 32):
+        ref, wref, _ = O.route(logits, bias, k)
+        ids, wts = K.kmoe_route(torch.from_numpy(logits).cuda(), torch.from_numpy(bias).cuda(), k)
+        assert np.array_equal(ids.cpu().numpy(), ref)
+        assert np.allclose(wts.cpu().numpy(), wref, rtol=1e-6)
+    E = 8
+    lg = np.random.default_rng(0).standard_normal((7, E)).astype(np.float32)
+    b = np.zeros(E, np.float32)
+    ref, _, _ = O.route(lg, b, E)
+    ids, _ = K.kmoe_route(torch.from_numpy(lg).cuda(), torch.from_numpy(b).cuda(), E)
+    assert np.array_equal(ids.cpu().numpy(), ref)
+
+
+def _quant_check(K, xbits, fmt):
+    x = torch.from_numpy(xbits.view(np.int16)).view(torch.bfloat16).cuda()
+    codes, scales = K.kmoe_quantize_mx(x, fmt)
+    xf = W.bf16_bits_to_f64(xbits)
+    name = "e4m3" if fmt == K.KMOE_MXFP8_E4M3 else "e2m1"
+    qref, sref = F.quantize_mx(xf, name)
+    if name == "e2m1":
+        qref = F.pack_e2m1(qref)
+    c = codes.cpu().numpy()
+    sc = scales.cpu().numpy()
+    assert np.array_equal(sc, sref), f"{(sc != sref).sum()} scale bytes differ"
+    assert np.array_equal(c, qref), f"{(c != qref).sum()} code bytes differ"
+
+
+@pytest.mark.parametrize("name", ["tiny", "reduced", "decode", "prefill"])
+def test_quantize_mxfp8_bit_exact(K, name):
+    w = W.WORKLOADS[name]
+    _quant_check(K, W.gen_x(w), K.KMOE_MXFP8_E4M3)
+
+
+def test_quantize_edge_cases(K):
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((64, 256)) * np.exp(rng.uniform(-30, 30, (64, 1)))).astype(np.float32)
+    x[0, :32] = 0.0                                   # all-zero group
+    x[1, 5] = np.inf                                  # inf group
+    x[2, 7] = -np.inf
+    x[3, 9] = np.nan                                  # NaN ignored by the absmax, becomes +0
+    x[4, :] = 1e-40                                   # bf16 subnormals
+    x[5, :] = 448.0                                   # exactly qmax
+    x[6, :] = -0.0
+    x[7, :32] = 3.0e38                                # near the bf16 maximum
+    x[8, 0] = 1.0
+    x[8, 1:32] = 2.0 ** -20                           # tiny next to a large value
+    bits = W.f32_to_bf16_bits(x)
+    bits[3, 9] = 0x7FC0
+    for fmt in (K.KMOE_MXFP8_E4M3, K.KMOE_MXFP4_E2M1):
+        _quant_check(K, bits, fmt)
+
+
+def test_quantize_mxfp4_bit_exact(K):
+    w = W.WORKLOADS["reduced"]
+    _quant_check(K, W.gen_x(w)[:64], K.KMOE_MXFP4_E2M1)
+
+
+def test_bounded_wait_timeout_keeps_context(K):
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    K.kmoe_selftest_wait_timeout(ws, 2000)
+    st, word = K.kmoe_device_error(ws)
+    assert st == 7 and (word & 1)
+    st, word = K.kmoe_device_error(ws)     # cleared
+    assert st == 0 and word == 0
+    # the context still works
+    ids, _ = K.kmoe_route(torch.zeros(2, 8, device="cuda"), torch.zeros(8, device="cuda"), 2)
+    assert ids.cpu().tolist() == [[0, 1], [0, 1]]
