@@ -1,0 +1,459 @@
+"""Benchmark of the Kimi-K3 routed-expert MoE layer forward on GB300.
+
+One step = one kmoe_forward over one batch: routing -> MXFP8 quantisation ->
+expert permutation -> FC1 (+SiTU +requant) -> FC2 -> combine, with the layer's
+inputs (x, router logits, correction bias) and the 896 experts' MXFP4 weights
+resident in HBM.  Headline: tokens/s of the T=8192 prefill-chunk layer
+(H=7168, I=3584, E=896, top-16), with TFLOP/s and the T=16 decode layer's
+microseconds per layer alongside.  Inputs are synthetic and seeded.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle (a deliberately slow program)
+on the host cores, on a bounded token sample per step.
+Under torchrun (N > 1) every rank runs its own replica of the layer (the path
+does not shard; replicas only) and rank 0 prints one JSON line with the
+whole-job throughput (tokens of all ranks / slowest rank's time).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "Kimi-K3 MoE layer tokens/s & TFLOP/s at T=8192; µs/layer at T=16 (1×GB300)"
+HEADLINE = "prefill"     # T=8192 layer
+DECODE = "decode"        # T=16 layer
+KERNEL_LAUNCHES_PER_STEP = 7  # route, rank, scan, quantise-scatter, FC1, FC2, combine
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def reduce_max(dist, v, device):
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (200 ms period)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def fc1_traffic_record():
+    """DRAM bytes per FC1 launch from a committed ncu summary, if the kernel
+    source it was taken on is unchanged (else null)."""
+    path = os.path.join(ROOT, "profiles", "fc1_dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    src = open(os.path.join(ROOT, "mxfp8_mxfp4_moe_gb300", "csrc", "gemm.cu"), "rb").read()
+    if rec.get("gemm_cu_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    return rec
+
+
+# ----------------------------------------------------------------------------- layer set-up
+class Layer:
+    def __init__(self, w: W.Workload, device, weights=None):
+        import torch
+        import mxfp8_mxfp4_moe_gb300 as K
+        self.K = K
+        self.w = w
+        self.device = device
+        s = W.gen_small_inputs(w)
+        self.host = s
+        self.x = torch.from_numpy(s["x"].view(np.int16)).view(torch.bfloat16).to(device)
+        self.logits = torch.from_numpy(s["logits"]).to(device)
+        self.bias = torch.from_numpy(s["bias"]).to(device)
+        self.p = K.make_params(w.T, w.H, w.I, w.E, w.k, w.situ_beta, w.situ_linear_beta, w.routed_scaling_factor)
+        if weights is None:
+            wts = W.gen_expert_weights_torch(w, device)
+            w13_sf_k, w2_sf_k = K.kmoe_prepare_weights(self.p, wts["w13_sf"], wts["w2_sf"])
+            del wts["w13_sf"], wts["w2_sf"]
+            weights = {"w13": wts["w13"], "w2": wts["w2"], "w13_sf_k": w13_sf_k, "w2_sf_k": w2_sf_k}
+        self.weights = weights
+        self.ws = torch.zeros(K.kmoe_workspace_size(self.p), dtype=torch.uint8, device=device)
+        self.out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=device)
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        for e in self.events:
+            e.record()
+        torch.cuda.synchronize()
+
+    def forward(self, stage_events=False, x=None, logits=None, bias=None, out=None):
+        wt = self.weights
+        self.K.kmoe_forward(self.p, self.x if x is None else x, self.logits if logits is None else logits,
+                            self.bias if bias is None else bias, wt["w13"], wt["w13_sf_k"], wt["w2"],
+                            wt["w2_sf_k"], out=self.out if out is None else out, workspace=self.ws,
+                            stage_events=self.events if stage_events else None)
+
+    def stage_ms(self):
+        ev = self.events
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(6)]
+
+    def touched_experts(self):
+        v = self.K.stage_views(self.p, self.ws)
+        return int((v["counts"] > 0).sum().item())
+
+    def check(self):
+        st, word = self.K.kmoe_device_error(self.ws)
+        if st != 0:
+            raise RuntimeError(f"device error {word:#x}")
+
+
+def time_layer(layer, steps, warmup, dist, device, clocks=None):
+    import torch
+    for _ in range(warmup):
+        layer.forward()
+    torch.cuda.synchronize()
+    layer.check()
+    stream = torch.cuda.current_stream()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    start.record(stream)
+    for _ in range(steps):
+        layer.forward()
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    barrier(dist)
+    total_ms = start.elapsed_time(end)
+    return total_ms, clk
+
+
+def time_stages(layer, steps):
+    """Per-stage durations from the stage events, averaged over `steps` forwards."""
+    import torch
+    acc = np.zeros(6)
+    for _ in range(steps):
+        layer.forward(stage_events=True)
+        torch.cuda.synchronize()
+        acc += np.array(layer.stage_ms())
+    return (acc / steps).tolist()
+
+
+def e2e_time(layer, steps, warmup):
+    """Same metric through the C ABI with host buffers: per step the H2D copy of
+    x, logits and bias from pinned memory, the forward, and the D2H read of the
+    output, all inside the timed region."""
+    import torch
+    hx = layer.x.cpu().pin_memory()
+    hl = layer.logits.cpu().pin_memory()
+    hb = layer.bias.cpu().pin_memory()
+    hout = torch.empty(layer.out.shape, dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(layer.x)
+    dl = torch.empty_like(layer.logits)
+    db = torch.empty_like(layer.bias)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        db.copy_(hb, non_blocking=True)
+        layer.forward(x=dx, logits=dl, bias=db)
+        hout.copy_(layer.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    h2d = hx.numel() * 2 + hl.numel() * 4 + hb.numel() * 4
+    d2h = hout.numel() * 2
+    return s.elapsed_time(e), h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_inputs(w: W.Workload):
+    from oracle import moe as O
+    s = W.gen_small_inputs(w)
+    ids, _, _ = O.route(s["logits"], s["bias"], w.k)
+    return s, ids
+
+
+def oracle_sample(w: W.Workload, budget_s: float = 12.0, seed: int = 7, pre=None):
+    """Time the float64 oracle (as it stands) on a bounded token sample of the
+    workload; returns (tokens/s, tokens, seconds, threads)."""
+    from oracle import moe as O
+    s, ids = pre if pre is not None else oracle_inputs(w)
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.T)
+    n = 1
+    done_tok, done_s = 0, 0.0
+    while done_s < budget_s and done_tok < w.T:
+        tokens = np.sort(order[done_tok:done_tok + n])
+        used = sorted(set(int(e) for e in ids[tokens].ravel()))
+        wts = W.gen_expert_weights_np(w, used)          # data generation: outside the timed region
+        t0 = time.perf_counter()
+        O.forward(w, s["x"], s["logits"], s["bias"], wts, experts_host=used, tokens=tokens, ids=None)
+        done_s += time.perf_counter() - t0
+        done_tok += len(tokens)
+        n = min(2 * n, 8)
+    return done_tok / done_s, done_tok, done_s, os.cpu_count()
+
+
+# ----------------------------------------------------------------------------- main
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[HEADLINE]
+    pre = oracle_inputs(w)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        tps, ntok, secs, cores = oracle_sample(w, budget_s=args.ref_step_s, seed=i, pre=pre)
+        if i >= args.warmup:
+            per_step.append((tps, ntok, secs))
+    tps = sum(x[1] for x in per_step) / sum(x[2] for x in per_step)
+    line = {
+        "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * w.T / tps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "impl": "reference",
+        "config": {"workload": "Kimi-K3 MoE layer prefill chunk T=8192 H=7168 I=3584 E=896 top-16",
+                   "global_batch": w.T, "seq_len": w.T, "parallelism": "replicas"},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sum(x[1] for x in per_step)} sampled tokens over {args.steps} steps "
+                                   f"(float64 numpy oracle, routing of all tokens plus the sampled tokens' experts)"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(ws, "nccl")
+    import mxfp8_mxfp4_moe_gb300 as K
+    st = K.kmoe_check_device(local)
+    if st != 0:
+        raise SystemExit(f"kmoe_check_device: {K.kmoe_status_string(st)}")
+    peaks, peaks_kind = measured_peaks()
+
+    # ---- headline: T=8192 prefill chunk
+    wp = W.WORKLOADS[HEADLINE]
+    layer = Layer(wp, device)
+    clocks = ClockSampler(local) if rank == 0 else None
+    total_ms, clk = time_layer(layer, args.steps, args.warmup, dist, device, clocks)
+    total_ms = reduce_max(dist, total_ms, device)
+    ms_step = total_ms / args.steps
+    tokens_s = ws * wp.T * args.steps / (total_ms / 1e3)
+    tflops = wp.flops() / (ms_step / 1e3) / 1e12
+    stages = time_stages(layer, max(3, min(args.steps, 10)))
+    layer.check()
+    fc1_ms = stages[3]
+    fc1_flops = 4.0 * wp.R * wp.H * wp.I
+    fc1_tf = fc1_flops / (fc1_ms / 1e3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    traffic = fc1_traffic_record()
+    e2e_ms, h2d, d2h = e2e_time(layer, args.steps, max(1, args.warmup // 2))
+    e2e_ms = reduce_max(dist, e2e_ms, device)
+    e2e_tok_s = ws * wp.T * args.steps / (e2e_ms / 1e3)
+    touched_p = layer.touched_experts()
+    weights = layer.weights
+    del layer
+    torch.cuda.empty_cache()
+
+    # ---- decode: T=16 (same experts, same weights)
+    wd = W.WORKLOADS[DECODE]
+    dl = Layer(wd, device, weights=weights)
+    d_total, _ = time_layer(dl, max(args.steps, 20), args.warmup, dist, device, None)
+    d_total = reduce_max(dist, d_total, device)
+    d_us = 1000.0 * d_total / max(args.steps, 20)
+    d_stages = time_stages(dl, 10)
+    touched = dl.touched_experts()
+    dl.check()
+    per_expert_w13 = 2 * wd.I * wd.H // 2 + 2 * wd.I * wd.H // 32
+    per_expert_all = wd.expert_weight_bytes()
+    d_fc1_gbs = touched * per_expert_w13 / (d_stages[3] / 1e3) / 1e9
+    d_layer_bytes = touched * per_expert_all + 2 * wd.T * wd.H * 2 + 4 * wd.T * wd.E
+    d_layer_gbs = d_layer_bytes / (d_us / 1e6) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, ntok, secs, cores = oracle_sample(wp, budget_s=args.cpu_budget_s)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{ntok} random tokens of the T=8192 layer ({secs:.1f} s of float64 oracle work: "
+                         f"routing of all tokens, then quantise/FC1/SiTU/requant/FC2/combine for the sample)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "mxfp8xmxfp4 (e4m3 x e2m1, ue8m0 scales, fp32 accumulate, bf16 out)",
+            "data": "synthetic (seeded; random MXFP4 weights of the Kimi-K3 expert shapes)",
+            "config": {"workload": "Kimi-K3 MoE layer prefill chunk T=8192 H=7168 I=3584 E=896 top-16 "
+                                   "(SiTU 4/25)", "global_batch": wp.T * ws, "seq_len": wp.T,
+                       "parallelism": "replicas" if ws > 1 else "single-gpu",
+                       "l2": "inputs larger than L2 (36.7 GB of expert weights streamed every step)",
+                       "tile_rows": K.kmoe_workspace_layout(layer_params(K, wp)).tile_rows,
+                       "touched_experts": touched_p},
+            "tflops": tflops,
+            "stages_ms": dict(zip(K.STAGE_NAMES, stages)),
+            "roofline": {"bound": "tensor", "kernel": "FC1 grouped GEMM (tcgen05 mxf8f6f4, SiTU+requant epilogue)",
+                         "achieved": fc1_tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": fc1_tf / fp8_peak,
+                         "peak_source": f"{peaks_kind}: 2 x bf16_tflops_sustained (nominal FP8/BF16 ratio 2)",
+                         "algorithmic": f"4*R*H*I = {fc1_flops:.4g} FLOP per launch",
+                         "traffic": (traffic["dram_bytes_per_launch"] if traffic else None)},
+            "decode": {"workload": "Kimi-K3 MoE layer decode T=16 H=7168 I=3584 E=896 top-16",
+                       "us_per_layer": d_us, "touched_experts": touched, "layer_GBs": d_layer_gbs,
+                       "layer_hbm_frac": d_layer_gbs / peaks["hbm_gbs"],
+                       "stages_us": {n: 1000 * v for n, v in zip(K.STAGE_NAMES, d_stages)},
+                       "roofline": {"bound": "hbm", "kernel": "FC1 grouped GEMM", "achieved": d_fc1_gbs,
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": d_fc1_gbs / peaks["hbm_gbs"],
+                                    "algorithmic": f"touched experts x {per_expert_w13} B of w13 codes+scales",
+                                    "traffic": None}},
+            "e2e": {"value": e2e_tok_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": KERNEL_LAUNCHES_PER_STEP * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "device": torch.cuda.get_device_name(device),
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_profile(args):
+    """Lean mode for profiler captures: one workload, warm-up + steps forwards,
+    stage times printed as JSON (no clocks, baselines or e2e)."""
+    import torch
+    torch.cuda.set_device(0)
+    w = {**W.WORKLOADS, **W.PROFILE_WORKLOADS}[args.profile]
+    layer = Layer(w, torch.device("cuda", 0))
+    for _ in range(args.warmup + args.steps):
+        layer.forward(stage_events=True)
+    torch.cuda.synchronize()
+    layer.check()
+    import mxfp8_mxfp4_moe_gb300 as K
+    print(json.dumps({"profile": w.name, "stages_ms": dict(zip(K.STAGE_NAMES, layer.stage_ms())),
+                      "touched_experts": layer.touched_experts(),
+                      "tile_rows": K.kmoe_workspace_layout(layer.p).tile_rows}))
+    return 0
+
+
+def layer_params(K, w):
+    return K.make_params(w.T, w.H, w.I, w.E, w.k, w.situ_beta, w.situ_linear_beta, w.routed_scaling_factor)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None, help="lean run of one workload (for profiler captures)")
+    args = ap.parse_args(argv)
+    if args.profile:
+        return run_profile(args)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -169,6 +169,21 @@ int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, 
                  const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace, size_t ws_bytes,
                  cudaStream_t stream);
 
+/* Events recorded on `stream` between the stages of kmoe_forward_ex (host
+ * struct of caller-created events; a null field is skipped).  Recorded in
+ * order: start, after routing (or the copy of the given routing), after the
+ * permutation, after the quantise-scatter, after FC1, after FC2, after the
+ * combine.  For profiling; the kernels launched are the same. */
+typedef struct kmoe_stage_events {
+  cudaEvent_t start, routed, permuted, quantized, fc1, fc2, combined;
+} kmoe_stage_events;
+
+/* kmoe_forward with optional stage events (ev may be null). */
+int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
+                    const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
+                    const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace,
+                    size_t ws_bytes, cudaStream_t stream, const kmoe_stage_events* ev /* host */);
+
 /* Reads the device error word of `workspace` (synchronises `stream`), clears
  * it, and returns KMOE_OK, KMOE_ERR_TIMEOUT or KMOE_ERR_DEVICE.  *word (host,
  * may be null) receives the raw bits (1: a bounded wait timed out, 2: an

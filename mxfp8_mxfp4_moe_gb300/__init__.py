@@ -25,7 +25,8 @@ KMOE_MXFP4_E2M1 = 1
 
 EXPORTS = ("kmoe_status_string", "kmoe_check_device", "kmoe_workspace_size", "kmoe_workspace_layout",
            "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_scale_bytes", "kmoe_prepare_weights",
-           "kmoe_forward", "kmoe_device_error", "kmoe_tile_sf_offset", "kmoe_selftest_wait_timeout")
+           "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error", "kmoe_tile_sf_offset",
+           "kmoe_selftest_wait_timeout")
 
 
 class kmoe_params(ctypes.Structure):
@@ -38,6 +39,14 @@ class kmoe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("err", "topk_ids", "topk_w", "counts", "seg_start", "tile_start",
                                                "row_of_slot", "slot_of_row", "xq", "xsf", "iq", "isf", "y")] + \
                [("tile_rows", ctypes.c_int), ("max_tiles", ctypes.c_int), ("total", ctypes.c_size_t)]
+
+
+class kmoe_stage_events(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("start", "routed", "permuted", "quantized", "fc1", "fc2",
+                                               "combined")]
+
+
+STAGE_NAMES = ("route", "permute", "quantize", "fc1", "fc2", "combine")
 
 
 class KmoeError(RuntimeError):
@@ -67,12 +76,14 @@ def load_library(path: str = LIB_PATH):
     lib.kmoe_prepared_scale_bytes.argtypes = [pp, I]
     lib.kmoe_prepare_weights.argtypes = [pp, P, P, P, P, V]
     lib.kmoe_forward.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, S, V]
+    lib.kmoe_forward_ex.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, S, V, ctypes.POINTER(kmoe_stage_events)]
     lib.kmoe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), V]
     lib.kmoe_tile_sf_offset.restype = S
     lib.kmoe_tile_sf_offset.argtypes = [I, I, I, I, I, I]
     lib.kmoe_selftest_wait_timeout.argtypes = [P, I, V]
     for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
-              "kmoe_prepare_weights", "kmoe_forward", "kmoe_device_error", "kmoe_selftest_wait_timeout"):
+              "kmoe_prepare_weights", "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error",
+              "kmoe_selftest_wait_timeout"):
         getattr(lib, n).restype = ctypes.c_int
     return lib
 
@@ -172,7 +183,8 @@ def kmoe_prepare_weights(p, w13_sf, w2_sf, stream=None):
 
 
 def kmoe_forward(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, topk_w=None, out=None,
-                 workspace=None, stream=None):
+                 workspace=None, stream=None, stage_events=None):
+    """stage_events: optional list of 7 torch.cuda.Event recorded between the stages (kmoe_forward_ex)."""
     _dev(x, "x", torch.bfloat16)
     for n, t in (("w13", w13), ("w13_sf_k", w13_sf_k), ("w2", w2), ("w2_sf_k", w2_sf_k)):
         _dev(t, n, torch.uint8)
@@ -186,9 +198,14 @@ def kmoe_forward(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, 
         out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
         workspace = torch.empty(kmoe_workspace_size(p), dtype=torch.uint8, device=x.device)
-    _check("kmoe_forward", _lib.kmoe_forward(
-        ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(w13_sf_k), _ptr(w2), _ptr(w2_sf_k),
-        _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    args = (ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(w13_sf_k), _ptr(w2),
+            _ptr(w2_sf_k), _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    if stage_events is None:
+        _check("kmoe_forward", _lib.kmoe_forward(*args))
+    else:
+        ev = kmoe_stage_events(*[e.cuda_event for e in stage_events])
+        _check("kmoe_forward_ex", _lib.kmoe_forward_ex(*args, ctypes.byref(ev)))
     return out, workspace
 
 

@@ -201,6 +201,14 @@ int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, 
                  const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
                  const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace, size_t ws_bytes,
                  cudaStream_t stream) {
+  return kmoe_forward_ex(p, x_bf16, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids, topk_w, out_bf16, workspace,
+                         ws_bytes, stream, nullptr);
+}
+
+int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
+                    const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
+                    const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace,
+                    size_t ws_bytes, cudaStream_t stream, const kmoe_stage_events* ev) {
   int st = check_params(p);
   if (st != KMOE_OK) return st;
   Layout L;
@@ -243,6 +251,8 @@ int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, 
       !make_map(&mB2, CU_TENSOR_MAP_DATA_TYPE_UINT8, iq, I, R, I, 128, 32))
     return KMOE_ERR_CUDA;
 
+  auto mark = [&](cudaEvent_t e) { return (ev && e) ? cudaEventRecord(e, stream) : cudaSuccess; };
+  KMOE_CK(mark(ev ? ev->start : nullptr));
   KMOE_CK(cudaMemsetAsync(err, 0, 16, stream));  // the error word reports this call only
   if (given) {
     KMOE_CK(cudaMemcpyAsync(ids, topk_ids, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
@@ -250,18 +260,24 @@ int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, 
   } else {
     KMOE_CK(launch_route(logits, bias, T, E, k, ids, wts, stream));
   }
+  KMOE_CK(mark(ev ? ev->routed : nullptr));
   KMOE_CK(launch_permute(ids, R, E, L.BN, rank, chunk_prefix, counts, seg_start, tile_start, err, stream));
+  KMOE_CK(mark(ev ? ev->permuted : nullptr));
   KMOE_CK(launch_quant_scatter(x_bf16, T, H, k, E, L.BN, L.nch, L.max_tiles, ids, rank, chunk_prefix, seg_start,
                                tile_start, row_of_slot, slot_of_row, xq, xsf, stream));
+  KMOE_CK(mark(ev ? ev->quantized : nullptr));
   const int grid = num_sms();
   if (grid <= 0) return KMOE_ERR_CUDA;
   GemmArgs a1{counts, seg_start, tile_start, w13_sf_k, xsf, E, I / 64, H / 128, L.max_tiles, H, I,
               iq, isf, p->situ_beta, p->situ_linear_beta, nullptr, slot_of_row, err, kWaitBudgetNs};
   KMOE_CK(launch_moe_gemm(true, L.BN, mA1, mB1, a1, grid, stream));
+  KMOE_CK(mark(ev ? ev->fc1 : nullptr));
   GemmArgs a2{counts, seg_start, tile_start, w2_sf_k, isf, E, H / 128, I / 128, L.max_tiles, H, I,
               nullptr, nullptr, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs};
   KMOE_CK(launch_moe_gemm(false, L.BN, mA2, mB2, a2, grid, stream));
+  KMOE_CK(mark(ev ? ev->fc2 : nullptr));
   KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));
+  KMOE_CK(mark(ev ? ev->combined : nullptr));
   return KMOE_OK;
 }
 

@@ -83,6 +83,14 @@ WORKLOADS = {
     "skewed": Workload("skewed", T=2048, H=7168, I=3584, E=896, k=16, skewed=True),
 }
 
+# Smaller cases of the same kernels, sized for profiler captures (a few GB on
+# the device, still larger than L2): a prefill-like layer with hundreds of rows
+# per touched expert, and a decode-like layer with one or two.
+PROFILE_WORKLOADS = {
+    "ncu_prefill": Workload("ncu_prefill", T=1536, H=7168, I=3584, E=64, k=16),
+    "ncu_decode": Workload("ncu_decode", T=16, H=7168, I=3584, E=64, k=16),
+}
+
 
 # ----------------------------------------------------------------------------
 # bf16 helpers (storage as uint16 bit patterns)
