@@ -203,6 +203,31 @@ size_t kmoe_tile_sf_offset(int tile, int local_row, int g, int tile_rows, int K,
  * kmoe_device_error, which must then return KMOE_ERR_TIMEOUT). */
 int kmoe_selftest_wait_timeout(void* workspace, int budget_us, cudaStream_t stream);
 
+/* Size of the scratch array built into the library for kmoe_forward_noalloc
+ * (32 MiB, reserved on every GPU that loads the library until the process
+ * exits). */
+#define KMOE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* kmoe_forward for callers that cannot allocate device memory -- for example
+ * a runtime that plans all GPU memory up front, or a plug-in that receives a
+ * stream but no allocator -- and so cannot pass a workspace.  The pages this
+ * library follows have no counterpart of this call; it is an integration aid.
+ * Arguments are those of kmoe_forward without the workspace; the caller still
+ * owns every input and output.  The workspace is a fixed array inside the
+ * library of KMOE_NOALLOC_SCRATCH_BYTES; layers whose kmoe_workspace_size()
+ * exceeds it are rejected with KMOE_ERR_WORKSPACE (small decode batches fit:
+ * T = 16 at H = 7168, I = 3584, E = 896, k = 16 needs about 21 MiB).  Nothing
+ * is allocated or freed.  The first call on a device looks up the array's
+ * device address with that device current; make that first call before any
+ * stream capture.  Every call uses the same array, which keeps the previous
+ * call's contents, so calls that can overlap on the GPU race: order them.
+ * device_error (device pointer, optional) receives the call's device error
+ * word (the bits kmoe_device_error reports) when the stream reaches it. */
+int kmoe_forward_noalloc(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
+                         const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
+                         const int32_t* topk_ids, const float* topk_w, void* out_bf16, uint32_t* device_error,
+                         cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

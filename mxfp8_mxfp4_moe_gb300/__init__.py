@@ -26,7 +26,8 @@ KMOE_MXFP4_E2M1 = 1
 EXPORTS = ("kmoe_status_string", "kmoe_check_device", "kmoe_workspace_size", "kmoe_workspace_layout",
            "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_scale_bytes", "kmoe_prepare_weights",
            "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error", "kmoe_tile_sf_offset",
-           "kmoe_selftest_wait_timeout")
+           "kmoe_selftest_wait_timeout", "kmoe_forward_noalloc")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class kmoe_params(ctypes.Structure):
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH):
     lib.kmoe_tile_sf_offset.restype = S
     lib.kmoe_tile_sf_offset.argtypes = [I, I, I, I, I, I]
     lib.kmoe_selftest_wait_timeout.argtypes = [P, I, V]
+    lib.kmoe_forward_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, V]
+    lib.kmoe_forward_noalloc.restype = ctypes.c_int
     for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
               "kmoe_prepare_weights", "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error",
               "kmoe_selftest_wait_timeout"):
@@ -207,6 +210,21 @@ def kmoe_forward(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, 
         ev = kmoe_stage_events(*[e.cuda_event for e in stage_events])
         _check("kmoe_forward_ex", _lib.kmoe_forward_ex(*args, ctypes.byref(ev)))
     return out, workspace
+
+
+def kmoe_forward_noalloc(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, topk_w=None, out=None,
+                         device_error=None, stream=None):
+    """kmoe_forward without a workspace argument, for hosts that cannot
+    allocate device memory: the library's built-in scratch array
+    (NOALLOC_SCRATCH_BYTES, shared by all calls) is used instead.  `out` and
+    the optional `device_error` (one int32 on the device) are caller-owned."""
+    _dev(x, "x", torch.bfloat16)
+    if out is None:
+        out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
+    _check("kmoe_forward_noalloc", _lib.kmoe_forward_noalloc(
+        ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(w13_sf_k), _ptr(w2), _ptr(w2_sf_k),
+        _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(device_error), _stream(stream)))
+    return out
 
 
 def kmoe_device_error(workspace, stream=None):
