@@ -156,9 +156,10 @@ class Layer:
         self.p = K.make_params(w.T, w.H, w.I, w.E, w.k, w.situ_beta, w.situ_linear_beta, w.routed_scaling_factor)
         if weights is None:
             wts = W.gen_expert_weights_torch(w, device)
-            w13_sf_k, w2_sf_k = K.kmoe_prepare_weights(self.p, wts["w13_sf"], wts["w2_sf"])
-            del wts["w13_sf"], wts["w2_sf"]
-            weights = {"w13": wts["w13"], "w2": wts["w2"], "w13_sf_k": w13_sf_k, "w2_sf_k": w2_sf_k}
+            w13_k, w2_k = K.kmoe_prepare_weights(self.p, wts["w13"], wts["w13_sf"], wts["w2"], wts["w2_sf"])
+            del wts
+            torch.cuda.empty_cache()
+            weights = {"w13_k": w13_k, "w2_k": w2_k}
         self.weights = weights
         self.ws = torch.zeros(K.kmoe_workspace_size(self.p), dtype=torch.uint8, device=device)
         self.out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=device)
@@ -170,8 +171,8 @@ class Layer:
     def forward(self, stage_events=False, x=None, logits=None, bias=None, out=None):
         wt = self.weights
         self.K.kmoe_forward(self.p, self.x if x is None else x, self.logits if logits is None else logits,
-                            self.bias if bias is None else bias, wt["w13"], wt["w13_sf_k"], wt["w2"],
-                            wt["w2_sf_k"], out=self.out if out is None else out, workspace=self.ws,
+                            self.bias if bias is None else bias, wt["w13_k"], wt["w2_k"],
+                            out=self.out if out is None else out, workspace=self.ws,
                             stage_events=self.events if stage_events else None)
 
     def stage_ms(self):

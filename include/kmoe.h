@@ -137,19 +137,26 @@ int kmoe_route(const float* logits, const float* bias, int T, int E, int k, int3
 int kmoe_quantize_mx(const void* x_bf16, int rows, int cols, int fmt, uint8_t* codes, uint8_t* scales,
                      cudaStream_t stream);
 
-/* Bytes of the re-laid-out weight scales (which = 0: w13, 1: w2); equal to
- * the raw scale bytes (E*2I*H/32 and E*H*I/32). */
-size_t kmoe_prepared_scale_bytes(const kmoe_params* p, int which);
+/* Bytes of the prepared weights (which = 0: FC1 / w13, 1: FC2 / w2):
+ * blocks of KMOE_WEIGHT_BLOCK_BYTES, one per (expert, 128-row weight tile,
+ * 128-wide K block): E*(I/64)*(H/128) blocks for w13 and E*(H/128)*(I/128)
+ * for w2 (the raw code + scale bytes, re-ordered). */
+#define KMOE_WEIGHT_BLOCK_BYTES (8192 + 512)
+size_t kmoe_prepared_weight_bytes(const kmoe_params* p, int which);
 
-/* One-time weight preparation (load time, not per forward): re-lays the
- * raw row-major UE8M0 weight scales into the order in which the GEMMs copy
- * them into tensor memory (per 128-row weight tile and per 128-wide K
- * block, a 512-byte block of 32 lanes x 4 rows x 4 K-groups).  The FP4
- * codes are used as given.
- *   w13_sf [E, 2I, H/32], w2_sf [E, H, I/32] raw (in);
- *   w13_sf_k, w2_sf_k (out, kmoe_prepared_scale_bytes each, 16-byte aligned). */
-int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13_sf, const uint8_t* w2_sf, uint8_t* w13_sf_k,
-                         uint8_t* w2_sf_k, cudaStream_t stream);
+/* One-time weight preparation (load time, not per forward; cf. the pages'
+ * process_weights_after_loading re-layout for the SM100 path).  Re-lays the
+ * raw checkpoint tensors into the order the GEMMs stream them: for each
+ * expert, each 128-row weight tile (FC1: gate rows 64m..64m+63 followed by
+ * the matching up rows I+64m..; FC2: rows 128m..128m+127) and each 128-wide K
+ * block, one contiguous block of 128 rows x 64 code bytes followed by the 512
+ * scale bytes of those rows (32 lanes x 4 rows x 4 K groups, the order in
+ * which tcgen05.cp copies scales into tensor memory).
+ *   w13 [E, 2I, H/2], w13_sf [E, 2I, H/32], w2 [E, H, I/2], w2_sf [E, H, I/32]
+ *   (raw, in; codes 16-byte aligned);
+ *   w13_k, w2_k (out, kmoe_prepared_weight_bytes each, 256-byte aligned). */
+int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
+                         const uint8_t* w2_sf, uint8_t* w13_k, uint8_t* w2_k, cudaStream_t stream);
 
 /* The routed-expert MoE forward:
  *   route (unless topk_ids/topk_w are given) -> MXFP8-quantise x ->
@@ -157,17 +164,15 @@ int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13_sf, const uint
  *   MXFP8 requantise -> FC2 (. w2^T) -> out[t] = bf16(rsf * sum_j w_j y_j)
  *   with slots summed in order j = 0..k-1 in fp32 (deterministic).
  * x [T, H] bf16 (16-byte aligned); logits/bias as kmoe_route (ignored when
- * topk_ids is given); w13/w2 codes 32-byte aligned; w13_sf_k/w2_sf_k from
- * kmoe_prepare_weights; topk_ids [T, k] int32 and topk_w [T, k] float
- * optional (both or neither; an id < 0 marks a masked slot that adds 0;
- * an id >= E raises KMOE_ERR_DEVICE via kmoe_device_error and is masked);
- * out [T, H] bf16 (16-byte aligned); workspace of kmoe_workspace_size(p)
- * bytes, 256-byte aligned, reused by every call (not thread-safe per
- * workspace). */
+ * topk_ids is given); w13_k/w2_k from kmoe_prepare_weights (256-byte
+ * aligned); topk_ids [T, k] int32 and topk_w [T, k] float optional (both or
+ * neither; an id < 0 marks a masked slot that adds 0; an id >= E raises
+ * KMOE_ERR_DEVICE via kmoe_device_error and is masked); out [T, H] bf16
+ * (16-byte aligned); workspace of kmoe_workspace_size(p) bytes, 256-byte
+ * aligned, reused by every call (not thread-safe per workspace). */
 int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
-                 const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
-                 const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace, size_t ws_bytes,
-                 cudaStream_t stream);
+                 const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
+                 void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Events recorded on `stream` between the stages of kmoe_forward_ex (host
  * struct of caller-created events; a null field is skipped).  Recorded in
@@ -180,9 +185,9 @@ typedef struct kmoe_stage_events {
 
 /* kmoe_forward with optional stage events (ev may be null). */
 int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
-                    const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
-                    const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace,
-                    size_t ws_bytes, cudaStream_t stream, const kmoe_stage_events* ev /* host */);
+                    const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
+                    void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                    const kmoe_stage_events* ev /* host */);
 
 /* Reads the device error word of `workspace` (synchronises `stream`), clears
  * it, and returns KMOE_OK, KMOE_ERR_TIMEOUT or KMOE_ERR_DEVICE.  *word (host,
@@ -224,9 +229,8 @@ int kmoe_selftest_wait_timeout(void* workspace, int budget_us, cudaStream_t stre
  * device_error (device pointer, optional) receives the call's device error
  * word (the bits kmoe_device_error reports) when the stream reaches it. */
 int kmoe_forward_noalloc(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
-                         const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
-                         const int32_t* topk_ids, const float* topk_w, void* out_bf16, uint32_t* device_error,
-                         cudaStream_t stream);
+                         const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
+                         void* out_bf16, uint32_t* device_error, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

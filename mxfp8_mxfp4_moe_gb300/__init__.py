@@ -24,7 +24,7 @@ KMOE_MXFP8_E4M3 = 0
 KMOE_MXFP4_E2M1 = 1
 
 EXPORTS = ("kmoe_status_string", "kmoe_check_device", "kmoe_workspace_size", "kmoe_workspace_layout",
-           "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_scale_bytes", "kmoe_prepare_weights",
+           "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_weight_bytes", "kmoe_prepare_weights",
            "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error", "kmoe_tile_sf_offset",
            "kmoe_selftest_wait_timeout", "kmoe_forward_noalloc")
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -73,16 +73,16 @@ def load_library(path: str = LIB_PATH):
     lib.kmoe_workspace_layout.argtypes = [pp, ctypes.POINTER(kmoe_ws_layout)]
     lib.kmoe_route.argtypes = [P, P, I, I, I, P, P, V]
     lib.kmoe_quantize_mx.argtypes = [P, I, I, I, P, P, V]
-    lib.kmoe_prepared_scale_bytes.restype = S
-    lib.kmoe_prepared_scale_bytes.argtypes = [pp, I]
-    lib.kmoe_prepare_weights.argtypes = [pp, P, P, P, P, V]
-    lib.kmoe_forward.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, S, V]
-    lib.kmoe_forward_ex.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, S, V, ctypes.POINTER(kmoe_stage_events)]
+    lib.kmoe_prepared_weight_bytes.restype = S
+    lib.kmoe_prepared_weight_bytes.argtypes = [pp, I]
+    lib.kmoe_prepare_weights.argtypes = [pp, P, P, P, P, P, P, V]
+    lib.kmoe_forward.argtypes = [pp, P, P, P, P, P, P, P, P, P, S, V]
+    lib.kmoe_forward_ex.argtypes = [pp, P, P, P, P, P, P, P, P, P, S, V, ctypes.POINTER(kmoe_stage_events)]
     lib.kmoe_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), V]
     lib.kmoe_tile_sf_offset.restype = S
     lib.kmoe_tile_sf_offset.argtypes = [I, I, I, I, I, I]
     lib.kmoe_selftest_wait_timeout.argtypes = [P, I, V]
-    lib.kmoe_forward_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, V]
+    lib.kmoe_forward_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, V]
     lib.kmoe_forward_noalloc.restype = ctypes.c_int
     for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
               "kmoe_prepare_weights", "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error",
@@ -171,26 +171,30 @@ def kmoe_quantize_mx(x, fmt=KMOE_MXFP8_E4M3, codes=None, scales=None, stream=Non
     return codes, scales
 
 
-def kmoe_prepare_weights(p, w13_sf, w2_sf, stream=None):
-    _dev(w13_sf, "w13_sf", torch.uint8)
-    _dev(w2_sf, "w2_sf", torch.uint8)
-    n13 = _lib.kmoe_prepared_scale_bytes(ctypes.byref(p), 0)
-    n2 = _lib.kmoe_prepared_scale_bytes(ctypes.byref(p), 1)
-    if n13 == 0 or w13_sf.numel() != n13 or w2_sf.numel() != n2:
-        raise ValueError("weight scale sizes do not match the parameters")
-    a = torch.empty(n13, dtype=torch.uint8, device=w13_sf.device)
-    b = torch.empty(n2, dtype=torch.uint8, device=w13_sf.device)
-    _check("kmoe_prepare_weights", _lib.kmoe_prepare_weights(ctypes.byref(p), _ptr(w13_sf), _ptr(w2_sf), _ptr(a),
-                                                             _ptr(b), _stream(stream)))
+def kmoe_prepared_weight_bytes(p, which):
+    return _lib.kmoe_prepared_weight_bytes(ctypes.byref(p), which)
+
+
+def kmoe_prepare_weights(p, w13, w13_sf, w2, w2_sf, stream=None):
+    """Raw checkpoint tensors -> (w13_k, w2_k) prepared weight blocks."""
+    for n, t in (("w13", w13), ("w13_sf", w13_sf), ("w2", w2), ("w2_sf", w2_sf)):
+        _dev(t, n, torch.uint8)
+    if (w13.numel() != p.E * 2 * p.I * p.H // 2 or w13_sf.numel() != p.E * 2 * p.I * p.H // 32 or
+            w2.numel() != p.E * p.H * p.I // 2 or w2_sf.numel() != p.E * p.H * p.I // 32):
+        raise ValueError("weight sizes do not match the parameters (w13 [E, 2I, H/2], w2 [E, H, I/2])")
+    a = torch.empty(kmoe_prepared_weight_bytes(p, 0), dtype=torch.uint8, device=w13.device)
+    b = torch.empty(kmoe_prepared_weight_bytes(p, 1), dtype=torch.uint8, device=w13.device)
+    _check("kmoe_prepare_weights", _lib.kmoe_prepare_weights(ctypes.byref(p), _ptr(w13), _ptr(w13_sf), _ptr(w2),
+                                                             _ptr(w2_sf), _ptr(a), _ptr(b), _stream(stream)))
     return a, b
 
 
-def kmoe_forward(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, topk_w=None, out=None,
-                 workspace=None, stream=None, stage_events=None):
+def kmoe_forward(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=None, out=None, workspace=None,
+                 stream=None, stage_events=None):
     """stage_events: optional list of 7 torch.cuda.Event recorded between the stages (kmoe_forward_ex)."""
     _dev(x, "x", torch.bfloat16)
-    for n, t in (("w13", w13), ("w13_sf_k", w13_sf_k), ("w2", w2), ("w2_sf_k", w2_sf_k)):
-        _dev(t, n, torch.uint8)
+    _dev(w13_k, "w13_k", torch.uint8)
+    _dev(w2_k, "w2_k", torch.uint8)
     if topk_ids is None:
         _dev(logits, "logits", torch.float32)
         _dev(bias, "bias", torch.float32)
@@ -201,9 +205,8 @@ def kmoe_forward(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, 
         out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
         workspace = torch.empty(kmoe_workspace_size(p), dtype=torch.uint8, device=x.device)
-    args = (ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(w13_sf_k), _ptr(w2),
-            _ptr(w2_sf_k), _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(),
-            _stream(stream))
+    args = (ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13_k), _ptr(w2_k), _ptr(topk_ids),
+            _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     if stage_events is None:
         _check("kmoe_forward", _lib.kmoe_forward(*args))
     else:
@@ -212,7 +215,7 @@ def kmoe_forward(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, 
     return out, workspace
 
 
-def kmoe_forward_noalloc(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids=None, topk_w=None, out=None,
+def kmoe_forward_noalloc(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=None, out=None,
                          device_error=None, stream=None):
     """kmoe_forward without a workspace argument, for hosts that cannot
     allocate device memory: the library's built-in scratch array
@@ -222,8 +225,8 @@ def kmoe_forward_noalloc(p, x, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_id
     if out is None:
         out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
     _check("kmoe_forward_noalloc", _lib.kmoe_forward_noalloc(
-        ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(w13_sf_k), _ptr(w2), _ptr(w2_sf_k),
-        _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(device_error), _stream(stream)))
+        ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13_k), _ptr(w2_k), _ptr(topk_ids), _ptr(topk_w),
+        _ptr(out), _ptr(device_error), _stream(stream)))
     return out
 
 

@@ -19,7 +19,6 @@ cudaError_t launch_quant_scatter(const void*, int, int, int, int, int, int, int,
                                  uint8_t*, cudaStream_t);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int, int, int, int, float, void*,
                            cudaStream_t);
-cudaError_t launch_prep_wsf(const uint8_t*, uint8_t*, int, int, int, int, int, int, int, cudaStream_t);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t budget_ns, cudaStream_t st);
 __global__ void kmoe_probe_kernel();
 }  // namespace kmoe
@@ -60,6 +59,26 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
   return fn(m, dt, 2, const_cast<void*>(base), gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map over the code region of prepared weights: [nblk][128 rows][128
+// E2M1 codes] (64 bytes per row, 8192 per block); a box holds `depth`
+// consecutive blocks (K blocks of one weight tile).
+bool make_weight_map(CUtensorMap* m, const void* base, uint64_t nblk, uint32_t depth) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3] = {128, 128, nblk};
+  cuuint64_t gstr[2] = {64, 8192};
+  cuuint32_t box[3] = {128, 128, depth};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), gdim, gstr, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t weight_blocks(const kmoe_params* p, int which) {
+  if (which == 0) return static_cast<size_t>(p->E) * (p->I / 64) * (p->H / 128);
+  return static_cast<size_t>(p->E) * (p->H / 128) * (p->I / 128);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -155,8 +174,8 @@ int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out) {
 }
 
 size_t kmoe_tile_sf_offset(int tile, int local_row, int g, int tile_rows, int K, int max_tiles) {
-  (void)K;
-  return tile_sf_offset(tile, local_row, g, (tile_rows + 127) / 128, max_tiles);
+  (void)max_tiles;
+  return tile_sf_offset(tile, local_row, g, (tile_rows + 127) / 128, K / 128);
 }
 
 int kmoe_route(const float* logits, const float* bias, int T, int E, int k, int32_t* topk_ids, float* topk_w,
@@ -179,36 +198,33 @@ int kmoe_quantize_mx(const void* x_bf16, int rows, int cols, int fmt, uint8_t* c
   return KMOE_OK;
 }
 
-size_t kmoe_prepared_scale_bytes(const kmoe_params* p, int which) {
-  if (check_params(p) != KMOE_OK) return 0;
-  if (which == 0) return static_cast<size_t>(p->E) * 2 * p->I * (p->H / 32);
-  if (which == 1) return static_cast<size_t>(p->E) * p->H * (p->I / 32);
-  return 0;
+size_t kmoe_prepared_weight_bytes(const kmoe_params* p, int which) {
+  if (check_params(p) != KMOE_OK || (which != 0 && which != 1)) return 0;
+  return weight_blocks(p, which) * kWeightBlockBytes;
 }
 
-int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13_sf, const uint8_t* w2_sf, uint8_t* w13_sf_k,
-                         uint8_t* w2_sf_k, cudaStream_t stream) {
+int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13, const uint8_t* w13_sf, const uint8_t* w2,
+                         const uint8_t* w2_sf, uint8_t* w13_k, uint8_t* w2_k, cudaStream_t stream) {
   int st = check_params(p);
   if (st != KMOE_OK) return st;
-  if (!w13_sf || !w2_sf || !w13_sf_k || !w2_sf_k) return KMOE_ERR_ARG;
-  if (!aligned(w13_sf_k, 16) || !aligned(w2_sf_k, 16)) return KMOE_ERR_ALIGN;
-  KMOE_CK(launch_prep_wsf(w13_sf, w13_sf_k, p->E, p->I / 64, p->H / 128, 2 * p->I, p->H / 32, 1, p->I, stream));
-  KMOE_CK(launch_prep_wsf(w2_sf, w2_sf_k, p->E, p->H / 128, p->I / 128, p->H, p->I / 32, 0, p->I, stream));
+  if (!w13 || !w13_sf || !w2 || !w2_sf || !w13_k || !w2_k) return KMOE_ERR_ARG;
+  if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_k, 256) || !aligned(w2_k, 256)) return KMOE_ERR_ALIGN;
+  KMOE_CK(launch_prep_weights(w13, w13_sf, w13_k, p->E, p->I / 64, p->H / 128, 2 * p->I, p->H, 1, p->I, stream));
+  KMOE_CK(launch_prep_weights(w2, w2_sf, w2_k, p->E, p->H / 128, p->I / 128, p->H, p->I, 0, p->I, stream));
   return KMOE_OK;
 }
 
 int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
-                 const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
-                 const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace, size_t ws_bytes,
-                 cudaStream_t stream) {
-  return kmoe_forward_ex(p, x_bf16, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids, topk_w, out_bf16, workspace,
-                         ws_bytes, stream, nullptr);
+                 const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
+                 void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return kmoe_forward_ex(p, x_bf16, logits, bias, w13_k, w2_k, topk_ids, topk_w, out_bf16, workspace, ws_bytes,
+                         stream, nullptr);
 }
 
 int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
-                    const uint8_t* w13, const uint8_t* w13_sf_k, const uint8_t* w2, const uint8_t* w2_sf_k,
-                    const int32_t* topk_ids, const float* topk_w, void* out_bf16, void* workspace,
-                    size_t ws_bytes, cudaStream_t stream, const kmoe_stage_events* ev) {
+                    const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
+                    void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                    const kmoe_stage_events* ev) {
   int st = check_params(p);
   if (st != KMOE_OK) return st;
   Layout L;
@@ -218,10 +234,9 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   if (p->T == 0) return KMOE_OK;
   const bool given = topk_ids != nullptr;
   if ((topk_ids == nullptr) != (topk_w == nullptr)) return KMOE_ERR_ARG;
-  if (!x_bf16 || !w13 || !w13_sf_k || !w2 || !w2_sf_k || !out_bf16) return KMOE_ERR_ARG;
+  if (!x_bf16 || !w13_k || !w2_k || !out_bf16) return KMOE_ERR_ARG;
   if (!given && (!logits || !bias)) return KMOE_ERR_ARG;
-  if (!aligned(x_bf16, 16) || !aligned(out_bf16, 16) || !aligned(w13, 32) || !aligned(w2, 32) ||
-      !aligned(w13_sf_k, 16) || !aligned(w2_sf_k, 16))
+  if (!aligned(x_bf16, 16) || !aligned(out_bf16, 16) || !aligned(w13_k, 256) || !aligned(w2_k, 256))
     return KMOE_ERR_ALIGN;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -243,13 +258,18 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   const int T = p->T, H = p->H, I = p->I, E = p->E, k = p->k, R = L.R;
 
   // tensor maps: weights as E2M1 (unpacked to 16-byte aligned groups in smem), token rows as bytes
-  CUtensorMap mA1, mA2, mB1, mB2;
-  if (!make_map(&mA1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, static_cast<uint64_t>(E) * 2 * I, H / 2, 128,
-                64) ||
-      !make_map(&mA2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, static_cast<uint64_t>(E) * H, I / 2, 128, 128) ||
-      !make_map(&mB1, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, H, R, H, 128, 32) ||
-      !make_map(&mB2, CU_TENSOR_MAP_DATA_TYPE_UINT8, iq, I, R, I, 128, 32))
+  const int kps1 = gemm_kblocks_per_stage(L.BN, H / 128);
+  const int kps2 = gemm_kblocks_per_stage(L.BN, I / 128);
+  GemmMaps m1, m2;
+  if (!make_weight_map(&m1.a, w13_k, weight_blocks(p, 0), kps1) ||
+      !make_weight_map(&m2.a, w2_k, weight_blocks(p, 1), kps2))
     return KMOE_ERR_CUDA;
+  for (int i = 0; i < 3; ++i) {
+    const uint32_t rows = 32u << i;  // 32, 64, 128-row boxes of token rows
+    if (!make_map(&m1.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, H, R, H, 128, rows) ||
+        !make_map(&m2.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, iq, I, R, I, 128, rows))
+      return KMOE_ERR_CUDA;
+  }
 
   auto mark = [&](cudaEvent_t e) { return (ev && e) ? cudaEventRecord(e, stream) : cudaSuccess; };
   KMOE_CK(mark(ev ? ev->start : nullptr));
@@ -268,13 +288,14 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   KMOE_CK(mark(ev ? ev->quantized : nullptr));
   const int grid = num_sms();
   if (grid <= 0) return KMOE_ERR_CUDA;
-  GemmArgs a1{counts, seg_start, tile_start, w13_sf_k, xsf, E, I / 64, H / 128, L.max_tiles, H, I,
-              iq, isf, p->situ_beta, p->situ_linear_beta, nullptr, slot_of_row, err, kWaitBudgetNs};
-  KMOE_CK(launch_moe_gemm(true, L.BN, mA1, mB1, a1, grid, stream));
+  GemmArgs a1{counts, seg_start, tile_start, w13_k, w13_k + weight_blocks(p, 0) * 8192, xsf, E, I / 64, H / 128,
+              L.max_tiles, H, I, iq, isf, p->situ_beta, p->situ_linear_beta, nullptr, slot_of_row, err,
+              kWaitBudgetNs};
+  KMOE_CK(launch_moe_gemm(true, L.BN, kps1, m1, a1, grid, stream));
   KMOE_CK(mark(ev ? ev->fc1 : nullptr));
-  GemmArgs a2{counts, seg_start, tile_start, w2_sf_k, isf, E, H / 128, I / 128, L.max_tiles, H, I,
-              nullptr, nullptr, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs};
-  KMOE_CK(launch_moe_gemm(false, L.BN, mA2, mB2, a2, grid, stream));
+  GemmArgs a2{counts, seg_start, tile_start, w2_k, w2_k + weight_blocks(p, 1) * 8192, isf, E, H / 128, I / 128,
+              L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs};
+  KMOE_CK(launch_moe_gemm(false, L.BN, kps2, m2, a2, grid, stream));
   KMOE_CK(mark(ev ? ev->fc2 : nullptr));
   KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));
   KMOE_CK(mark(ev ? ev->combined : nullptr));

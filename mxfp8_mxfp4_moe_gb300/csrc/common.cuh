@@ -17,15 +17,15 @@ constexpr int kMaxK = 32;
 // ---------------------------------------------------------------- tile layout
 // Scales of the B operand (token rows) are stored per token tile so that a
 // tile's scales for one 128-wide K block form whole 512-byte blocks that
-// tcgen05.cp copies into TMEM at a 4-aligned column:
-//   block (kb, tile, chunk) = 512 bytes, chunk = local_row / 128,
+// tcgen05.cp copies into TMEM at a 4-aligned column, and the blocks of
+// consecutive K blocks of one tile are contiguous (one copy per stage):
+//   block (tile, kb, chunk) = 512 bytes, chunk = local_row / 128,
 //   byte j*16 + c*4 + g%4 holds row 32c + j (of the chunk) for K group g.
-__host__ __device__ __forceinline__ size_t tile_sf_offset(int tile, int local_row, int g, int nch, int max_tiles) {
+__host__ __device__ __forceinline__ size_t tile_sf_offset(int tile, int local_row, int g, int nch, int KB) {
   const int kb = g >> 2;
   const int chunk = local_row >> 7;
   const int r = local_row & 127;
-  return ((static_cast<size_t>(kb) * max_tiles + tile) * nch + chunk) * 512 + (r & 31) * 16 + (r >> 5) * 4 +
-         (g & 3);
+  return ((static_cast<size_t>(tile) * KB + kb) * nch + chunk) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (g & 3);
 }
 
 // ---------------------------------------------------------------- workspace

@@ -13,10 +13,17 @@
 // lane quarters), fp32 accumulators in TMEM.  Weights sit in the M=128 slot
 // so a tile holds as few as 16 routed rows (decode) and up to BN (prefill).
 //
-// Warp roles (192 threads, persistent, one CTA per SM):
+// Weights are read from the load-time layout of kmoe_prepare_weights: per
+// (expert, 128-row weight tile, 128-wide K block) one contiguous block of
+// 8192 code bytes (128 rows x 64 B) followed by its 512 scale bytes, blocks
+// ordered by K block.  A work item therefore streams one contiguous range.
+//
+// Warp roles (320 threads, persistent, one CTA per SM):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2..5  epilogue; warp w reads TMEM lane quarter w % 4
+//   warps 2..9  epilogue in two groups of four; warp w reads TMEM lane
+//               quarter w % 4, group g = (w - 2) / 4 takes the 32-column
+//               chunks 2i + g of the tile
 // Pipelines: STAGES smem stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (acc_full/acc_empty) so the epilogue of one work item
 // overlaps the main loop of the next.  Every wait is bounded.
@@ -31,20 +38,26 @@
 
 namespace kmoe {
 
-
-
-template <int BN_, int STAGES_, bool FC1_>
+template <int BN_, int KPS_, int STAGES_, bool FC1_>
 struct GemmCfg {
   static constexpr int BN = BN_;
+  static constexpr int KPS = KPS_;        // 128-wide K blocks per pipeline stage
   static constexpr int STAGES = STAGES_;
   static constexpr bool FC1 = FC1_;
-  static constexpr int A_BYTES = 16384;  // 128 rows x 128 FP4 in the unpacked smem format
-  static constexpr int A_TX = 8192;      // transaction bytes of that tile (packed source)
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int A_KB = 16384;     // 128 rows x 128 FP4 in the unpacked smem format
+  static constexpr int A_TX_KB = 8192;   // transaction bytes of that tile (packed source)
+  static constexpr int B_KB = BN * 128;  // token rows x 128 E4M3
   static constexpr int NCH = (BN + 127) / 128;
-  static constexpr int SF_OFF = A_BYTES + B_BYTES;
-  static constexpr int STAGE = (A_BYTES + B_BYTES + 512 + NCH * 512 + 1023) / 1024 * 1024;
-  static constexpr int STG_BYTES = FC1 ? 128 * 33 * 4 : 0;
+  static constexpr int B_OFF = KPS * A_KB;
+  static constexpr int SFA_OFF = B_OFF + KPS * B_KB;
+  static constexpr int SFB_OFF = SFA_OFF + KPS * 512;
+  static constexpr int STAGE = (SFB_OFF + KPS * NCH * 512 + 1023) / 1024 * 1024;
+  static constexpr int SFW = 4 + 4 * NCH;  // TMEM scale columns per K block (A, then B chunks)
+  static_assert(KPS * SFW <= 16, "scale columns per stage");
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int STG_FLOATS = 128 * 33;  // one 128 x 32 staging tile (padded rows) per group
+  static constexpr int STG_BYTES = FC1 ? 2 * STG_FLOATS * 4 : 0;
   static constexpr int BAR_OFF = STAGES * STAGE + STG_BYTES;
   static constexpr int SMEM = 1024 + BAR_OFF + 256;
   static constexpr int SF_COL0 = 2 * BN;
@@ -89,16 +102,25 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads
   return out != 0;
 }
 
+// SiTU(g, u) = beta*tanh(g/beta)*sigmoid(g) * beta_lin*tanh(u/beta_lin), in fp32,
+// from exponentials of non-positive arguments only:
+//   tanh(v/b) = sign(v) * (1 - q)/(1 + q),  q = exp(-2|v|/b), 1 - q = -expm1(-2|v|/b)
+//   sigmoid(g) = 1/(1 + r) (g >= 0) or r/(1 + r) (g < 0),  r = exp(-|g|)
+// so the whole product is one quotient (no cancellation, no overflow).
 __device__ __forceinline__ float situ_f32(float g, float u, float beta, float beta_lin) {
-  const float gate = beta * tanhf(g / beta) * (1.0f / (1.0f + expf(-g)));
-  const float up = beta_lin * tanhf(u / beta_lin);
-  return gate * up;
+  const float ag = fabsf(g), au = fabsf(u);
+  const float eg = expm1f(-2.0f * ag / beta);      // in (-1, 0]
+  const float eu = expm1f(-2.0f * au / beta_lin);  // in (-1, 0]
+  const float r = expf(-ag);
+  const float num = (eg * eu) * (g >= 0.0f ? 1.0f : r);
+  const float den = ((2.0f + eg) * (2.0f + eu)) * (1.0f + r);
+  const float mag = (beta * beta_lin) * (num / den);
+  return ((g < 0.0f) != (u < 0.0f)) ? -mag : mag;
 }
 
 template <class C>
-__global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
-                                                          const __grid_constant__ CUtensorMap mapB,
-                                                          const GemmArgs a) {
+__global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmMaps maps,
+                                                                 const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -108,7 +130,6 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   uint64_t* done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* stg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -119,7 +140,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], C::EPI_WARPS);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -130,8 +151,8 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&mapA);
-    prefetch_tmap(&mapB);
+    prefetch_tmap(&maps.a);
+    for (int i = 0; i < 3; ++i) prefetch_tmap(&maps.b[i]);
   }
   tc_fence_before();
   __syncthreads();
@@ -143,27 +164,19 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_w = policy_evict_normal();
       const uint64_t pol_x = policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Work wk;
         decode_work(a, C::BN, w, wk);
-        const int ng = (wk.n + 31) >> 5;
-        const int nch = (wk.n + 127) >> 7;
-        const uint32_t tx = C::A_TX + ng * 4096 + 512 + nch * 512;
-        const uint8_t* wsf = a.wsf + (static_cast<size_t>(wk.e) * a.MT + wk.m) * a.KB * 512;
-        const uint8_t* bsf = a.bsf + static_cast<size_t>(wk.tile) * C::NCH * 512;
-        const size_t bsf_kb = static_cast<size_t>(a.max_tiles) * C::NCH * 512;
-        int rowA0, rowA1 = 0;
-        if (C::FC1) {
-          rowA0 = wk.e * 2 * a.I + 64 * wk.m;
-          rowA1 = rowA0 + a.I;
-        } else {
-          rowA0 = wk.e * a.H + 128 * wk.m;
-        }
-        for (int kb = 0; kb < a.KB; ++kb, ++it) {
+        const int ng = (wk.n + 31) >> 5;  // 32-row groups of the token tile
+        const uint32_t tx = C::KPS * (C::A_TX_KB + ng * 4096 + 512 + C::NCH * 512);
+        const int blk0 = (wk.e * a.MT + wk.m) * a.KB;
+        const uint8_t* wsf = a.wsf + static_cast<size_t>(blk0) * 512;
+        const uint8_t* bsf = a.bsf + static_cast<size_t>(wk.tile) * a.KB * C::NCH * 512;
+        for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
@@ -172,16 +185,23 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
           }
           uint8_t* st = smem + s * C::STAGE;
           mbar_arrive_expect_tx(&full[s], tx);
-          if (C::FC1) {
-            tma_load_2d(st, &mapA, &full[s], kb * 128, rowA0, pol_w);
-            tma_load_2d(st + 8192, &mapA, &full[s], kb * 128, rowA1, pol_w);
-          } else {
-            tma_load_2d(st, &mapA, &full[s], kb * 128, rowA0, pol_w);
+          tma_load_3d(st, &maps.a, &full[s], 0, 0, blk0 + kb, pol_w);
+#pragma unroll
+          for (int kbi = 0; kbi < C::KPS; ++kbi) {
+            // the tile's token rows in boxes of 128, 64 and 32 rows
+            uint8_t* sb = st + C::B_OFF + kbi * C::B_KB;
+            int g = 0;
+            for (int lv = 2; lv >= 0; --lv) {
+              const int rows_g = 1 << lv;
+              while (ng - g >= rows_g) {
+                tma_load_2d(sb + g * 4096, &maps.b[lv], &full[s], (kb + kbi) * 128, wk.r0 + 32 * g, pol_x);
+                g += rows_g;
+              }
+            }
           }
-          for (int b = 0; b < ng; ++b)
-            tma_load_2d(st + C::A_BYTES + b * 4096, &mapB, &full[s], kb * 128, wk.r0 + 32 * b, pol_x);
-          bulk_load(st + C::SF_OFF, wsf + static_cast<size_t>(kb) * 512, 512, &full[s]);
-          bulk_load(st + C::SF_OFF + 512, bsf + kb * bsf_kb, nch * 512, &full[s]);
+          bulk_load(st + C::SFA_OFF, wsf + static_cast<size_t>(kb) * 512, C::KPS * 512, &full[s]);
+          bulk_load(st + C::SFB_OFF, bsf + static_cast<size_t>(kb) * C::NCH * 512, C::KPS * C::NCH * 512,
+                    &full[s]);
         }
       }
       if (!ok) {
@@ -206,7 +226,7 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
         const uint32_t d = tmem + acc * C::BN;
         const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
         const int nch = (wk.n + 127) >> 7;
-        for (int kb = 0; kb < a.KB; ++kb, ++it) {
+        for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
           if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
@@ -215,16 +235,21 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
           }
           tc_fence_after();
           uint8_t* st = smem + s * C::STAGE;
-          const uint32_t sfc = tmem + C::SF_COL0 + s * 16;
-          tc_cp_32x128b_warpx4(sfc, sdesc_sf_32x16(smem_u32(st + C::SF_OFF)));
-          for (int c = 0; c < nch; ++c)
-            tc_cp_32x128b_warpx4(sfc + 4 + 4 * c, sdesc_sf_32x16(smem_u32(st + C::SF_OFF + 512 + 512 * c)));
-          const uint32_t aaddr = smem_u32(st);
-          const uint32_t baddr = smem_u32(st + C::A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_mxf8f6f4(d, sdesc_kmajor_sw128(aaddr + 32 * kk), sdesc_kmajor_sw128(baddr + 32 * kk),
-                         idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, kk, kk), sfc, sfc + 4, (kb | kk) != 0);
+          for (int kbi = 0; kbi < C::KPS; ++kbi) {
+            const uint32_t sfc = tmem + C::SF_COL0 + s * 16 + kbi * C::SFW;
+            tc_cp_32x128b_warpx4(sfc, sdesc_sf_32x16(smem_u32(st + C::SFA_OFF + kbi * 512)));
+            for (int c = 0; c < nch; ++c)
+              tc_cp_32x128b_warpx4(sfc + 4 + 4 * c,
+                                   sdesc_sf_32x16(smem_u32(st + C::SFB_OFF + (kbi * C::NCH + c) * 512)));
+            const uint32_t aaddr = smem_u32(st + kbi * C::A_KB);
+            const uint32_t baddr = smem_u32(st + C::B_OFF + kbi * C::B_KB);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              mma_mxf8f6f4(d, sdesc_kmajor_sw128(aaddr + 32 * kk), sdesc_kmajor_sw128(baddr + 32 * kk),
+                           idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, kk, kk), sfc, sfc + 4,
+                           (kb | kbi | kk) != 0);
+            }
           }
           tc_commit(&empty[s]);
         }
@@ -237,7 +262,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;   // TMEM lane quarter of this warp
-    const int eq = warp - 2;  // 0..3
+    const int ew = warp - 2;  // 0..7
+    const int grp = ew >> 2;  // chunk group
+    const int eq = ew & 3;    // warp within the group
+    float* stg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE) + grp * C::STG_FLOATS;
     uint32_t li = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++li) {
       Work wk;
@@ -245,11 +273,11 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
       const uint32_t acc = li & 1u;
       const uint32_t aph = (li >> 1) & 1u;
       bool ok = mbar_wait_bounded(&acc_full[acc], aph, budget, a.err, abort_flag);
-      ok = named_barrier_and(1, 128, ok && !*abort_flag);
+      ok = named_barrier_and(1, 32 * C::EPI_WARPS, ok && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::BN;
-      for (int c0 = 0; c0 < wk.n; c0 += 32) {
+      for (int c0 = 32 * grp; c0 < wk.n; c0 += 64) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c0, r);
         tmem_ld_wait();
@@ -267,16 +295,16 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
           float* row = stg + (32 * q + lane) * 33;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) row[jj] = __uint_as_float(r[jj]);
-          named_barrier(2, 128);
+          named_barrier(2 + grp, 128);
 #pragma unroll 1
           for (int cc = 0; cc < 8; ++cc) {
             const int cl = 8 * eq + cc;
             const int col = c0 + cl;
             if (col >= wk.n) break;
 #pragma unroll
-            for (int grp = 0; grp < 2; ++grp) {
-              const float g = stg[(32 * grp + lane) * 33 + cl];
-              const float u = stg[(64 + 32 * grp + lane) * 33 + cl];
+            for (int gh = 0; gh < 2; ++gh) {
+              const float g = stg[(32 * gh + lane) * 33 + cl];
+              const float u = stg[(64 + 32 * gh + lane) * 33 + cl];
               const float act = situ_f32(g, u, a.beta, a.beta_lin);
               float amax = fabsf(act);
 #pragma unroll
@@ -284,13 +312,13 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
               const int e = e4m3_scale_exp(amax);
               const uint8_t code = static_cast<uint8_t>(
                   __nv_cvt_float_to_fp8(act * exp2i(-e), __NV_SATFINITE, __NV_E4M3));
-              a.iq[static_cast<size_t>(wk.r0 + col) * a.I + 64 * wk.m + 32 * grp + lane] = code;
+              a.iq[static_cast<size_t>(wk.r0 + col) * a.I + 64 * wk.m + 32 * gh + lane] = code;
               if (lane == 0)
-                a.isf[tile_sf_offset(wk.tile, col, 2 * wk.m + grp, C::NCH, a.max_tiles)] =
+                a.isf[tile_sf_offset(wk.tile, col, 2 * wk.m + gh, C::NCH, a.I / 128)] =
                     static_cast<uint8_t>(e + 127);
             }
           }
-          named_barrier(2, 128);
+          named_barrier(2 + grp, 128);
         }
       }
       tc_fence_before();
@@ -306,60 +334,91 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
   }
 }
 
-// ---------------------------------------------------------------- weight scale re-layout
-// out[((e*MT + m)*KB + kb)*512 + j*16 + c*4 + g] = scale of weight-tile row
-// 32c+j for K group 4kb+g.  FC1 tile m holds gate rows 64m..64m+63 then up
-// rows I+64m..I+64m+63; FC2 tile m holds rows 128m..128m+127.
-__global__ void prep_wsf_kernel(const uint8_t* __restrict__ sf, uint8_t* __restrict__ out, int E, int MT, int KB,
-                                int rows_per_expert, int gpr, int fc1, int I) {
-  const size_t total = static_cast<size_t>(E) * MT * KB * 512;
+// ---------------------------------------------------------------- weight re-layout
+// Block (e, m, kb) of the prepared weights = 128 tile rows x 64 code bytes
+// (K elements 128kb..128kb+127 of each row) at blk*8192 in the code region,
+// and 512 scale bytes at nblk*8192 + blk*512 in the scale region, byte
+// j*16 + c*4 + g holding tile row 32c+j for K group 4kb+g.  FC1 tile m holds
+// gate rows 64m..64m+63 then up rows I+64m..I+64m+63; FC2 tile m holds rows
+// 128m..128m+127.  Blocks are ordered (e, m, kb).
+__device__ __forceinline__ int tile_row_src(int fc1, int m, int tr, int I) {
+  if (fc1) return tr < 64 ? 64 * m + tr : I + 64 * m + (tr - 64);
+  return 128 * m + tr;
+}
+
+__global__ void prep_weights_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
+                                    uint8_t* __restrict__ out, int E, int MT, int KB, int rows_per_expert, int K,
+                                    int fc1, int I) {
+  // one thread per 16 bytes of a block (8192 code bytes = 512 x 16, scales = 32 x 16)
+  constexpr int kPieces = kWeightBlockBytes / 16;
+  const size_t nblk = static_cast<size_t>(E) * MT * KB;
+  const size_t total = nblk * kPieces;
+  const size_t row_bytes = static_cast<size_t>(K) / 2;
+  const int gpr = K / 32;
   for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int byte = static_cast<int>(idx & 511);
-    size_t rest = idx >> 9;
-    const int kb = static_cast<int>(rest % KB);
-    rest /= KB;
-    const int m = static_cast<int>(rest % MT);
-    const int e = static_cast<int>(rest / MT);
-    const int j = byte >> 4, c = (byte >> 2) & 3, g = byte & 3;
-    const int tr = 32 * c + j;
-    int row;
-    if (fc1) row = tr < 64 ? 64 * m + tr : I + 64 * m + (tr - 64);
-    else row = 128 * m + tr;
-    out[idx] = sf[(static_cast<size_t>(e) * rows_per_expert + row) * gpr + 4 * kb + g];
+    const size_t blk = idx / kPieces;
+    const int piece = static_cast<int>(idx % kPieces);
+    const int kb = static_cast<int>(blk % KB);
+    const int m = static_cast<int>((blk / KB) % MT);
+    const int e = static_cast<int>(blk / (static_cast<size_t>(KB) * MT));
+    if (piece < 512) {
+      uint8_t* dst = out + blk * 8192 + static_cast<size_t>(piece) * 16;
+      const int tr = piece >> 2;
+      const int src_row = tile_row_src(fc1, m, tr, I);
+      const uint8_t* src =
+          codes + (static_cast<size_t>(e) * rows_per_expert + src_row) * row_bytes + kb * 64 + (piece & 3) * 16;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    } else {
+      const int j = piece - 512;  // lane j: rows j, 32+j, 64+j, 96+j
+      uint8_t* dst = out + nblk * 8192 + blk * 512 + static_cast<size_t>(j) * 16;
+      uint32_t v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int src_row = tile_row_src(fc1, m, 32 * c + j, I);
+        const uint8_t* s = sf + (static_cast<size_t>(e) * rows_per_expert + src_row) * gpr + 4 * kb;
+        v[c] = static_cast<uint32_t>(s[0]) | (static_cast<uint32_t>(s[1]) << 8) |
+               (static_cast<uint32_t>(s[2]) << 16) | (static_cast<uint32_t>(s[3]) << 24);
+      }
+      *reinterpret_cast<uint4*>(dst) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
   }
 }
 
-cudaError_t launch_prep_wsf(const uint8_t* sf, uint8_t* out, int E, int MT, int KB, int rows_per_expert, int gpr,
-                            int fc1, int I, cudaStream_t st) {
-  prep_wsf_kernel<<<1024, 256, 0, st>>>(sf, out, E, MT, KB, rows_per_expert, gpr, fc1, I);
+cudaError_t launch_prep_weights(const uint8_t* codes, const uint8_t* sf, uint8_t* out, int E, int MT, int KB,
+                                int rows_per_expert, int K, int fc1, int I, cudaStream_t st) {
+  prep_weights_kernel<<<2048, 256, 0, st>>>(codes, sf, out, E, MT, KB, rows_per_expert, K, fc1, I);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- launch
 template <class C>
-static cudaError_t launch_one(const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmArgs& a, int grid,
-                              cudaStream_t st) {
+static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st) {
   static bool attr_set = false;  // per instantiation; benign race (idempotent)
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  moe_gemm_kernel<C><<<grid, 192, C::SMEM, st>>>(mapA, mapB, a);
+  moe_gemm_kernel<C><<<grid, C::THREADS, C::SMEM, st>>>(maps, a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_moe_gemm(bool fc1, int BN, const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmArgs& a,
-                            int grid, cudaStream_t st) {
+cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, const GemmArgs& a, int grid,
+                            cudaStream_t st) {
+  if (a.KB % kps != 0) return cudaErrorInvalidValue;
   if (fc1) {
-    if (BN == 32) return launch_one<GemmCfg<32, 8, true>>(mapA, mapB, a, grid, st);
-    if (BN == 64) return launch_one<GemmCfg<64, 7, true>>(mapA, mapB, a, grid, st);
-    if (BN == 224) return launch_one<GemmCfg<224, 4, true>>(mapA, mapB, a, grid, st);
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 4, true>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<32, 1, 8, true>>(maps, a, grid, st);
+    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 3, true>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<64, 1, 6, true>>(maps, a, grid, st);
+    if (BN == 224 && kps == 1) return launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
   } else {
-    if (BN == 32) return launch_one<GemmCfg<32, 8, false>>(mapA, mapB, a, grid, st);
-    if (BN == 64) return launch_one<GemmCfg<64, 7, false>>(mapA, mapB, a, grid, st);
-    if (BN == 224) return launch_one<GemmCfg<224, 4, false>>(mapA, mapB, a, grid, st);
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 4, false>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<32, 1, 8, false>>(maps, a, grid, st);
+    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 4, false>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<64, 1, 7, false>>(maps, a, grid, st);
+    if (BN == 224 && kps == 1) return launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -4,11 +4,27 @@
 
 namespace kmoe {
 
+// One prepared weight block: 128 tile rows x 64 code bytes + 512 scale bytes
+// (codes of all blocks first, then the scales of all blocks).
+constexpr int kWeightBlockBytes = 8192 + 512;
+
+// Tensor maps of one grouped GEMM: the weight codes (box of kps K blocks)
+// and the token rows in boxes of 32, 64 and 128 rows.
+struct GemmMaps {
+  CUtensorMap a;
+  CUtensorMap b[3];
+};
+
+// K blocks (of 128) moved per pipeline stage for a token-tile size and a K
+// of KB blocks: two for the small tiles when KB is even, else one.
+inline int gemm_kblocks_per_stage(int BN, int KB) { return (BN <= 64 && KB % 2 == 0) ? 2 : 1; }
+
 struct GemmArgs {
   const int32_t* counts;      // [E]
   const int32_t* seg_start;   // [E+1]
   const int32_t* tile_start;  // [E+1]
-  const uint8_t* wsf;         // prepared weight scales [E][MT][KB][512]
+  const uint8_t* wq;          // prepared weight codes: [E][MT][KB] blocks of 128 rows x 64 B
+  const uint8_t* wsf;         // prepared weight scales: [E][MT][KB] blocks of 512 B
   const uint8_t* bsf;         // token-tile-layout scales of the B rows
   int E, MT, KB, max_tiles;
   int H, I;
@@ -23,9 +39,14 @@ struct GemmArgs {
   unsigned long long budget_ns;
 };
 
+// Re-lays raw codes [E, rows, K/2] and scales [E, rows, K/32] into prepared blocks.
+cudaError_t launch_prep_weights(const uint8_t* codes, const uint8_t* sf, uint8_t* out, int E, int MT, int KB,
+                                int rows_per_expert, int K, int fc1, int I, cudaStream_t st);
+
 // fc1: FC1 with the SiTU + MXFP8 requantisation epilogue; otherwise FC2 with
 // fp32 per-slot stores.  BN is the token-tile size of the layer (32, 64, 224).
-cudaError_t launch_moe_gemm(bool fc1, int BN, const CUtensorMap& mapA, const CUtensorMap& mapB, const GemmArgs& a,
-                            int grid, cudaStream_t st);
+// kps must equal gemm_kblocks_per_stage(BN, a.KB) (the depth of maps.a's box).
+cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, const GemmArgs& a, int grid,
+                            cudaStream_t st);
 
 }  // namespace kmoe

@@ -48,17 +48,16 @@ cudaError_t scratch_address(void** out) {
 }  // namespace
 
 extern "C" int kmoe_forward_noalloc(const kmoe_params* p, const void* x_bf16, const float* logits,
-                                    const float* bias, const uint8_t* w13, const uint8_t* w13_sf_k,
-                                    const uint8_t* w2, const uint8_t* w2_sf_k, const int32_t* topk_ids,
-                                    const float* topk_w, void* out_bf16, uint32_t* device_error,
-                                    cudaStream_t stream) {
+                                    const float* bias, const uint8_t* w13_k, const uint8_t* w2_k,
+                                    const int32_t* topk_ids, const float* topk_w, void* out_bf16,
+                                    uint32_t* device_error, cudaStream_t stream) {
   const size_t need = kmoe_workspace_size(p);
   if (need == 0) return KMOE_ERR_ARG;
   if (need > kScratchBytes) return KMOE_ERR_WORKSPACE;  // layer too large for the built-in scratch
   void* ws = nullptr;
   if (scratch_address(&ws) != cudaSuccess) return KMOE_ERR_CUDA;
-  const int st = kmoe_forward(p, x_bf16, logits, bias, w13, w13_sf_k, w2, w2_sf_k, topk_ids, topk_w, out_bf16, ws,
-                              kScratchBytes, stream);
+  const int st = kmoe_forward(p, x_bf16, logits, bias, w13_k, w2_k, topk_ids, topk_w, out_bf16, ws, kScratchBytes,
+                              stream);
   if (st != KMOE_OK) return st;
   if (device_error != nullptr) {
     // the error word sits at the start of the workspace

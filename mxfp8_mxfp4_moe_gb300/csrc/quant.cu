@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
       uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(row) * H + 32 * g);
       dst[0] = lo;
       dst[1] = hi;
-      xsf[tile_sf_offset(s_tile[j], s_local[j], g, nch, max_tiles)] = static_cast<uint8_t>(e + 127);
+      xsf[tile_sf_offset(s_tile[j], s_local[j], g, nch, H / 128)] = static_cast<uint8_t>(e + 127);
     }
   }
 }

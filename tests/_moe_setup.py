@@ -25,8 +25,10 @@ def device_weights(w: W.Workload, device="cuda"):
         torch.cuda.empty_cache()
         wts = W.gen_expert_weights_torch(w, device)
         p = params(w)
-        w13_sf_k, w2_sf_k = K.kmoe_prepare_weights(p, wts["w13_sf"], wts["w2_sf"])
-        _WEIGHT_CACHE[key] = dict(wts, w13_sf_k=w13_sf_k, w2_sf_k=w2_sf_k)
+        w13_k, w2_k = K.kmoe_prepare_weights(p, wts["w13"], wts["w13_sf"], wts["w2"], wts["w2_sf"])
+        del wts
+        torch.cuda.empty_cache()
+        _WEIGHT_CACHE[key] = {"w13_k": w13_k, "w2_k": w2_k}
     return _WEIGHT_CACHE[key]
 
 
@@ -52,8 +54,8 @@ def run_forward(w, small=None, topk_ids=None, topk_w=None, device="cuda"):
     wt = device_weights(w, device)
     inp, s = device_inputs(w, small, device)
     p = params(w)
-    out, ws = K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13"], wt["w13_sf_k"], wt["w2"],
-                             wt["w2_sf_k"], topk_ids=topk_ids, topk_w=topk_w)
+    out, ws = K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13_k"], wt["w2_k"], topk_ids=topk_ids,
+                             topk_w=topk_w)
     torch.cuda.synchronize()
     st, word = K.kmoe_device_error(ws)
     assert st == 0, f"device error word {word:#x}"
@@ -87,13 +89,13 @@ def assert_output_parity(gpu_bf16, ref, tag=""):
     assert mx <= 1e-2, f"{tag} max abs error {mx:.3e} x max|ref| > 1e-2"
 
 
-def tile_sf_offsets(tile, local, g, BN, max_tiles):
-    """Byte offsets in a token-tile scale array (layout plumbing, see include/kmoe.h)."""
+def tile_sf_offsets(tile, local, g, BN, KB):
+    """Byte offsets in a token-tile scale array (layout plumbing; kmoe_tile_sf_offset)."""
     nch = (BN + 127) // 128
     kb = g // 4
     chunk = local // 128
     r = local % 128
-    return ((kb * max_tiles + tile) * nch + chunk) * 512 + (r % 32) * 16 + (r // 32) * 4 + (g % 4)
+    return ((tile * KB + kb) * nch + chunk) * 512 + (r % 32) * 16 + (r // 32) * 4 + (g % 4)
 
 
 def gather_row_scales(sf_bytes: np.ndarray, views_np, rows: np.ndarray, K: int):
@@ -108,7 +110,7 @@ def gather_row_scales(sf_bytes: np.ndarray, views_np, rows: np.ndarray, K: int):
     tile = ts[e] + local // L.tile_rows
     lr = local % L.tile_rows
     g = np.arange(K // 32)
-    off = tile_sf_offsets(tile[:, None], lr[:, None], g[None, :], L.tile_rows, L.max_tiles)
+    off = tile_sf_offsets(tile[:, None], lr[:, None], g[None, :], L.tile_rows, K // 128)
     return sf_bytes[off]
 
 

@@ -52,8 +52,7 @@ def test_host_side_argument_errors(K):
            K.make_params(-1, 128, 128, 8, 2)]
     for p in bad:
         assert K.kmoe_workspace_size(p) == 0
-        st = lib.kmoe_forward(ctypes.byref(p), None, None, None, None, None, None, None, None, None, None, None, 0,
-                              None)
+        st = lib.kmoe_forward(ctypes.byref(p), None, None, None, None, None, None, None, None, None, 0, None)
         assert st in (1, 2)
     assert lib.kmoe_route(None, None, 4, 8, 9, None, None, None) == 1
     assert lib.kmoe_quantize_mx(None, 4, 100, 0, None, None, None) == 2
@@ -61,11 +60,13 @@ def test_host_side_argument_errors(K):
     p = K.make_params(16, 128, 128, 8, 2)
     n = K.kmoe_workspace_size(p)
     # workspace too small / misaligned pointers are rejected before any CUDA call
-    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 32, 16, 32, 16, None, None, 16, 256, n - 1, None) == 5
-    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 32, 16, 32, 16, None, None, 16, 258, n, None) == 3
-    assert lib.kmoe_forward(ctypes.byref(p), 8, 16, 16, 32, 16, 32, 16, None, None, 16, 256, n, None) == 3
-    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 16, 16, 32, 16, None, None, 16, 256, n, None) == 3
-    assert lib.kmoe_tile_sf_offset(1, 33, 5, 32, 128, 10) == ((1 * 10 + 1) * 1 + 0) * 512 + 1 * 16 + 1 * 4 + 1
+    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 256, 256, None, None, 16, 256, n - 1, None) == 5
+    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 256, 256, None, None, 16, 258, n, None) == 3
+    assert lib.kmoe_forward(ctypes.byref(p), 8, 16, 16, 256, 256, None, None, 16, 256, n, None) == 3
+    assert lib.kmoe_forward(ctypes.byref(p), 16, 16, 16, 128, 256, None, None, 16, 256, n, None) == 3
+    assert K.kmoe_prepared_weight_bytes(p, 0) == 8 * 2 * 1 * 8704 and K.kmoe_prepared_weight_bytes(p, 1) == 8 * 8704
+    # tile 1, row 33, group 5 (K block 1) of K = 256 (2 K blocks), 32-row tiles
+    assert lib.kmoe_tile_sf_offset(1, 33, 5, 32, 256, 10) == ((1 * 2 + 1) * 1 + 0) * 512 + 1 * 16 + 1 * 4 + 1
 
 
 def test_weight_generator_numpy_equals_torch():

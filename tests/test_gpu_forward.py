@@ -93,8 +93,7 @@ def test_determinism_and_graph_replay(K):
         outs = []
         for _ in range(3):
             o = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
-            K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13"], wt["w13_sf_k"], wt["w2"],
-                           wt["w2_sf_k"], out=o, workspace=ws)
+            K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13_k"], wt["w2_k"], out=o, workspace=ws)
             outs.append(o)
         torch.cuda.synchronize()
         for o in outs[1:]:
@@ -106,8 +105,8 @@ def test_determinism_and_graph_replay(K):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(graph, stream=stream):
-                K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13"], wt["w13_sf_k"], wt["w2"],
-                               wt["w2_sf_k"], out=g_out, workspace=ws, stream=stream)
+                K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13_k"], wt["w2_k"], out=g_out,
+                               workspace=ws, stream=stream)
         for _ in range(2):
             g_out.zero_()
             graph.replay()
@@ -142,7 +141,7 @@ def test_single_token_and_out_of_range_id(K):
     wts = torch.tensor([[0.5, 0.5]], dtype=torch.float32, device="cuda")
     wt = device_weights(w)
     inp, _ = device_inputs(w, s)
-    o, ws = K.kmoe_forward(p, inp["x"], None, None, wt["w13"], wt["w13_sf_k"], wt["w2"], wt["w2_sf_k"],
+    o, ws = K.kmoe_forward(p, inp["x"], None, None, wt["w13_k"], wt["w2_k"],
                            topk_ids=ids, topk_w=wts)
     st, word = K.kmoe_device_error(ws)
     assert st == 8 and (word & 2)

@@ -31,15 +31,13 @@ def _pair(K, w, seed):
     s = W.gen_small_inputs(w, seed=seed)
     inp, _ = device_inputs(w, s)
     p = params(w)
-    ref, ws = K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13"], wt["w13_sf_k"], wt["w2"],
-                             wt["w2_sf_k"])
+    ref, ws = K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13_k"], wt["w2_k"])
     out = torch.full((w.T, w.H), float("nan"), dtype=torch.bfloat16, device="cuda")
     err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     lib = K.lib()
     st = lib.kmoe_forward_noalloc(ctypes.byref(p), ctypes.c_void_p(inp["x"].data_ptr()),
                                   ctypes.c_void_p(inp["logits"].data_ptr()), ctypes.c_void_p(inp["bias"].data_ptr()),
-                                  ctypes.c_void_p(wt["w13"].data_ptr()), ctypes.c_void_p(wt["w13_sf_k"].data_ptr()),
-                                  ctypes.c_void_p(wt["w2"].data_ptr()), ctypes.c_void_p(wt["w2_sf_k"].data_ptr()),
+                                  ctypes.c_void_p(wt["w13_k"].data_ptr()), ctypes.c_void_p(wt["w2_k"].data_ptr()),
                                   None, None, ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(err.data_ptr()),
                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
@@ -62,6 +60,5 @@ def test_noalloc_matches_forward_twice(K, w):
 def test_noalloc_rejects_layers_beyond_its_scratch(K):
     p = K.make_params(8192, 7168, 3584, 896, 16)
     assert K.kmoe_workspace_size(p) > K.NOALLOC_SCRATCH_BYTES
-    st = K.lib().kmoe_forward_noalloc(ctypes.byref(p), None, None, None, None, None, None, None, None, None, None,
-                                      None, None)
+    st = K.lib().kmoe_forward_noalloc(ctypes.byref(p), None, None, None, None, None, None, None, None, None, None)
     assert st == 5  # KMOE_ERR_WORKSPACE
