@@ -18,12 +18,14 @@
 // 8192 code bytes (128 rows x 64 B) followed by its 512 scale bytes, blocks
 // ordered by K block.  A work item therefore streams one contiguous range.
 //
-// Warp roles (320 threads, persistent, one CTA per SM):
-//   warp 0      TMA producer (one lane)
+// Warp roles (persistent; one CTA per SM, two for the 32-row decode tiles):
+//   warp 0      TMA producer of the weight codes and scales (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2..9  epilogue in two groups of four; warp w reads TMEM lane
+//   warps 2..   epilogue, EPI_WARPS in groups of four; warp w reads TMEM lane
 //               quarter w % 4, group g = (w - 2) / 4 takes the 32-column
-//               chunks 2i + g of the tile
+//               chunks NGRP*i + g of the tile
+//   last warp   TMA producer of the token rows and their scales (one lane)
+// Two producer warps keep more bulk copies in flight than one thread can.
 // Pipelines: STAGES smem stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (acc_full/acc_empty) so the epilogue of one work item
 // overlaps the main loop of the next.  Every wait is bounded.
@@ -38,12 +40,13 @@
 
 namespace kmoe {
 
-template <int BN_, int KPS_, int STAGES_, bool FC1_>
+template <int BN_, int KPS_, int STAGES_, bool FC1_, int EPI_WARPS_ = 8, int CTAS_PER_SM_ = 1>
 struct GemmCfg {
   static constexpr int BN = BN_;
   static constexpr int KPS = KPS_;        // 128-wide K blocks per pipeline stage
   static constexpr int STAGES = STAGES_;
   static constexpr bool FC1 = FC1_;
+  static constexpr int CTAS_PER_SM = CTAS_PER_SM_;
   static constexpr int A_KB = 16384;     // 128 rows x 128 FP4 in the unpacked smem format
   static constexpr int A_TX_KB = 8192;   // transaction bytes of that tile (packed source)
   static constexpr int B_KB = BN * 128;  // token rows x 128 E4M3
@@ -54,10 +57,12 @@ struct GemmCfg {
   static constexpr int STAGE = (SFB_OFF + KPS * NCH * 512 + 1023) / 1024 * 1024;
   static constexpr int SFW = 4 + 4 * NCH;  // TMEM scale columns per K block (A, then B chunks)
   static_assert(KPS * SFW <= 16, "scale columns per stage");
-  static constexpr int EPI_WARPS = 8;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int EPI_WARPS = EPI_WARPS_;  // a multiple of 4 (one warp per TMEM lane quarter)
+  static constexpr int NGRP = EPI_WARPS / 4;      // epilogue groups (column-chunk interleave)
+  static constexpr int PRODB_WARP = 2 + EPI_WARPS;  // second producer: token rows and their scales
+  static constexpr int THREADS = 32 * (3 + EPI_WARPS);
   static constexpr int STG_FLOATS = 128 * 33;  // one 128 x 32 staging tile (padded rows) per group
-  static constexpr int STG_BYTES = FC1 ? 2 * STG_FLOATS * 4 : 0;
+  static constexpr int STG_BYTES = FC1 ? NGRP * STG_FLOATS * 4 : 0;
   static constexpr int BAR_OFF = STAGES * STAGE + STG_BYTES;
   static constexpr int SMEM = 1024 + BAR_OFF + 256;
   static constexpr int SF_COL0 = 2 * BN;
@@ -66,7 +71,9 @@ struct GemmCfg {
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static_assert(BN % 32 == 0 && BN <= 256, "token tile must be a multiple of 32 rows, at most 256");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SMEM * CTAS_PER_SM <= 232448, "shared memory budget");
+  static_assert(TMEM_COLS * CTAS_PER_SM <= 512, "TMEM budget per SM");
+  static_assert(EPI_WARPS % 4 == 0, "epilogue warps cover the four lane quarters");
 };
 
 struct Work {
@@ -119,7 +126,7 @@ __device__ __forceinline__ float situ_f32(float g, float u, float beta, float be
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmMaps maps,
+__global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(const __grid_constant__ GemmMaps maps,
                                                                  const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // one arrival per producer warp
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.a);
-    for (int i = 0; i < 3; ++i) prefetch_tmap(&maps.b[i]);
+    for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.b[i]);
   }
   tc_fence_before();
   __syncthreads();
@@ -161,18 +168,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
   const int total = a.MT * __ldg(a.tile_start + a.E);
   const uint64_t budget = a.budget_ns;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == C::PRODB_WARP) {
+    // ------------------------------------------------------------ producers
+    // warp 0: weight codes and scales; warp PRODB_WARP: token rows and their
+    // scales.  Both arrive on the stage's full barrier with their own bytes.
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_normal();
-      const uint64_t pol_x = policy_evict_last();
+      const bool is_a = warp == 0;
+      const uint64_t pol = is_a ? policy_evict_normal() : policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Work wk;
         decode_work(a, C::BN, w, wk);
         const int ng = (wk.n + 31) >> 5;  // 32-row groups of the token tile
-        const uint32_t tx = C::KPS * (C::A_TX_KB + ng * 4096 + 512 + C::NCH * 512);
+        const uint32_t tx = is_a ? C::KPS * (C::A_TX_KB + 512) : C::KPS * (ng * 4096 + C::NCH * 512);
         const int blk0 = (wk.e * a.MT + wk.m) * a.KB;
         const uint8_t* wsf = a.wsf + static_cast<size_t>(blk0) * 512;
         const uint8_t* bsf = a.bsf + static_cast<size_t>(wk.tile) * a.KB * C::NCH * 512;
@@ -185,23 +194,30 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
           }
           uint8_t* st = smem + s * C::STAGE;
           mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_3d(st, &maps.a, &full[s], 0, 0, blk0 + kb, pol_w);
+          if (is_a) {
+            tma_load_3d(st, &maps.a, &full[s], 0, 0, blk0 + kb, pol);
+            bulk_load(st + C::SFA_OFF, wsf + static_cast<size_t>(kb) * 512, C::KPS * 512, &full[s]);
+          } else {
 #pragma unroll
-          for (int kbi = 0; kbi < C::KPS; ++kbi) {
-            // the tile's token rows in boxes of 128, 64 and 32 rows
-            uint8_t* sb = st + C::B_OFF + kbi * C::B_KB;
-            int g = 0;
-            for (int lv = 2; lv >= 0; --lv) {
-              const int rows_g = 1 << lv;
-              while (ng - g >= rows_g) {
-                tma_load_2d(sb + g * 4096, &maps.b[lv], &full[s], (kb + kbi) * 128, wk.r0 + 32 * g, pol_x);
-                g += rows_g;
+            for (int kbi = 0; kbi < C::KPS; ++kbi) {
+              uint8_t* sb = st + C::B_OFF + kbi * C::B_KB;
+              const int x = (kb + kbi) * 128;
+              if (ng == C::BN / 32) {
+                tma_load_2d(sb, &maps.b[3], &full[s], x, wk.r0, pol);  // a whole tile in one box
+              } else {
+                int g = 0;  // the tile's token rows in boxes of 128, 64 and 32 rows
+                for (int lv = 2; lv >= 0; --lv) {
+                  const int rows_g = 1 << lv;
+                  while (ng - g >= rows_g) {
+                    tma_load_2d(sb + g * 4096, &maps.b[lv], &full[s], x, wk.r0 + 32 * g, pol);
+                    g += rows_g;
+                  }
+                }
               }
             }
+            bulk_load(st + C::SFB_OFF, bsf + static_cast<size_t>(kb) * C::NCH * 512, C::KPS * C::NCH * 512,
+                      &full[s]);
           }
-          bulk_load(st + C::SFA_OFF, wsf + static_cast<size_t>(kb) * 512, C::KPS * 512, &full[s]);
-          bulk_load(st + C::SFB_OFF, bsf + static_cast<size_t>(kb) * C::NCH * 512, C::KPS * C::NCH * 512,
-                    &full[s]);
         }
       }
       if (!ok) {
@@ -259,10 +275,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
       tc_commit(done);
       mbar_wait_bounded(done, 0, budget, a.err, nullptr);
     }
-  } else {
+  } else if (warp < C::PRODB_WARP) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;   // TMEM lane quarter of this warp
-    const int ew = warp - 2;  // 0..7
+    const int ew = warp - 2;  // 0..EPI_WARPS-1
     const int grp = ew >> 2;  // chunk group
     const int eq = ew & 3;    // warp within the group
     float* stg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE) + grp * C::STG_FLOATS;
@@ -277,7 +293,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::BN;
-      for (int c0 = 32 * grp; c0 < wk.n; c0 += 64) {
+      for (int c0 = 32 * grp; c0 < wk.n; c0 += 32 * C::NGRP) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c0, r);
         tmem_ld_wait();
@@ -400,7 +416,7 @@ static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& a, int grid,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  moe_gemm_kernel<C><<<grid, C::THREADS, C::SMEM, st>>>(maps, a);
+  moe_gemm_kernel<C><<<grid * C::CTAS_PER_SM, C::THREADS, C::SMEM, st>>>(maps, a);
   return cudaGetLastError();
 }
 
@@ -408,13 +424,13 @@ cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, con
                             cudaStream_t st) {
   if (a.KB % kps != 0) return cudaErrorInvalidValue;
   if (fc1) {
-    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 4, true>>(maps, a, grid, st)
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, true, 4, 2>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<32, 1, 8, true>>(maps, a, grid, st);
     if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 3, true>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<64, 1, 6, true>>(maps, a, grid, st);
     if (BN == 224 && kps == 1) return launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
   } else {
-    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 4, false>>(maps, a, grid, st)
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<32, 1, 8, false>>(maps, a, grid, st);
     if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 4, false>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<64, 1, 7, false>>(maps, a, grid, st);

@@ -9,10 +9,10 @@ namespace kmoe {
 constexpr int kWeightBlockBytes = 8192 + 512;
 
 // Tensor maps of one grouped GEMM: the weight codes (box of kps K blocks)
-// and the token rows in boxes of 32, 64 and 128 rows.
+// and the token rows in boxes of 32, 64, 128 rows and of one whole tile.
 struct GemmMaps {
   CUtensorMap a;
-  CUtensorMap b[3];
+  CUtensorMap b[4];
 };
 
 // K blocks (of 128) moved per pipeline stage for a token-tile size and a K
