@@ -289,12 +289,14 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   const int grid = num_sms();
   if (grid <= 0) return KMOE_ERR_CUDA;
   GemmArgs a1{counts, seg_start, tile_start, w13_k, w13_k + weight_blocks(p, 0) * 8192, xsf, E, I / 64, H / 128,
-              L.max_tiles, H, I, iq, isf, p->situ_beta, p->situ_linear_beta, nullptr, slot_of_row, err,
-              kWaitBudgetNs};
+              L.max_tiles, H, I, iq, isf, static_cast<float>(2.0 / p->situ_beta),
+              static_cast<float>(2.0 / p->situ_linear_beta),
+              static_cast<float>(static_cast<double>(p->situ_beta) * p->situ_linear_beta), nullptr, slot_of_row,
+              err, kWaitBudgetNs};
   KMOE_CK(launch_moe_gemm(true, L.BN, kps1, m1, a1, grid, stream));
   KMOE_CK(mark(ev ? ev->fc1 : nullptr));
   GemmArgs a2{counts, seg_start, tile_start, w2_k, w2_k + weight_blocks(p, 1) * 8192, isf, E, H / 128, I / 128,
-              L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs};
+              L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs};
   KMOE_CK(launch_moe_gemm(false, L.BN, kps2, m2, a2, grid, stream));
   KMOE_CK(mark(ev ? ev->fc2 : nullptr));
   KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));

@@ -2,7 +2,8 @@
 // Kimi-K3 SM120 FlashInfer MXFP4 page, Phase 2):
 //   out[t, h] = bf16_rn( rsf * sum_{j=0..k-1} w[t, j] * y[t*k + j, h] )
 // summed in fp32 in slot order; slots with a negative expert id are skipped.
-// One block per token, 16-byte loads of the fp32 rows.
+// Blocks cover (token, slice of H): enough blocks to fill the GPU even for a
+// handful of tokens; 16-byte loads of the fp32 rows.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -14,14 +15,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       __nv_bfloat16* __restrict__ out) {
   __shared__ float s_w[kMaxK];
   const int t = blockIdx.x;
+  const int H4 = H / 4;
+  const int h_begin = blockIdx.y * blockDim.x;  // one float4 per thread per slice
   if (threadIdx.x < k) {
     const int id = ids[static_cast<size_t>(t) * k + threadIdx.x];
     s_w[threadIdx.x] = (id >= 0 && id < E) ? w[static_cast<size_t>(t) * k + threadIdx.x] : 0.f;
   }
   __syncthreads();
   const float4* y4 = reinterpret_cast<const float4*>(y + static_cast<size_t>(t) * k * H);
-  const int H4 = H / 4;
-  for (int h = threadIdx.x; h < H4; h += blockDim.x) {
+  for (int h = h_begin + threadIdx.x; h < H4; h += blockDim.x * gridDim.y) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const float wj = s_w[j];
@@ -44,7 +46,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const float* y, const int32_t* ids, const float* w, int T, int H, int k, int E, float rsf,
                            void* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 256, 0, st>>>(y, ids, w, H, k, E, rsf, static_cast<__nv_bfloat16*>(out));
+  const int slices = (H / 4 + 255) / 256;
+  const int split = T >= 1024 ? 1 : slices;  // few tokens: one block per (token, H slice)
+  combine_kernel<<<dim3(T, split), 256, 0, st>>>(y, ids, w, H, k, E, rsf, static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 

@@ -31,7 +31,7 @@ struct GemmArgs {
   // FC1 epilogue
   uint8_t* iq;   // [R, I] E4M3 codes of SiTU output
   uint8_t* isf;  // token-tile-layout scales (K = I)
-  float beta, beta_lin;
+  float kg, ku, bb;            // SiTU: 2/situ_beta, 2/situ_linear_beta, situ_beta*situ_linear_beta
   // FC2 epilogue
   float* y;                   // [T*k, H]
   const int32_t* slot_of_row;  // [R]

@@ -69,22 +69,43 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     kth = bk;
   }
-  // pass 2: exact keys for the candidates
+  // pass 2: exact keys for the candidates.  Each lane evaluates one candidate
+  // per round (all lanes in step), so the double-precision work per warp is
+  // the largest candidate count of any lane rather than the candidate total.
   const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
   const float cut = (kth == NEG_INF) ? NEG_INF : kth - margin;
+  uint32_t cand = 0;
   float sx[KPL];
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = lane + 32 * i;
     sx[i] = 0.f;
-    if (e < E && key[i] >= cut) {
-      sx[i] = sigmoid_exact_f32(lgt[i]);
-      const float kx = sx[i] + b[i];
-      key[i] = isnan(kx) ? NEG_INF : kx;
-    } else {
-      key[i] = NEG_INF;
-    }
+    if (e < E && key[i] >= cut) cand |= 1u << i;
   }
+  const uint32_t cand0 = cand;
+  while (__any_sync(0xffffffffu, cand != 0)) {
+    const int pick = cand ? __ffs(cand) - 1 : -1;
+    float lv = 0.f, bv = 0.f;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i)
+      if (i == pick) {
+        lv = lgt[i];
+        bv = b[i];
+      }
+    const float sv = sigmoid_exact_f32(lv);
+    float kx = sv + bv;
+    if (isnan(kx)) kx = NEG_INF;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i)
+      if (i == pick) {
+        sx[i] = sv;
+        key[i] = kx;
+      }
+    if (pick >= 0) cand &= cand - 1;
+  }
+#pragma unroll
+  for (int i = 0; i < KPL; ++i)
+    if (!((cand0 >> i) & 1u)) key[i] = NEG_INF;  // not a candidate: cannot be chosen
   taken = 0;
   float mys = 0.f;
   int myid = -1;
