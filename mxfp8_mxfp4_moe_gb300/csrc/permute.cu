@@ -61,11 +61,17 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ chunk_
   int rows = 0, tiles = 0;
   for (int e = e0; e < e0 + per && e < E; ++e) {
     int run = 0;
-    for (int c = 0; c < nchunk; ++c) {
-      int32_t* p = chunk_counts + static_cast<size_t>(c) * E + e;
-      const int v = *p;
-      *p = run;
-      run += v;
+    // batches of independent loads, then the running prefix (keeps loads in flight)
+    for (int c0 = 0; c0 < nchunk; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = (c0 + i < nchunk) ? chunk_counts[static_cast<size_t>(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (c0 + i < nchunk) chunk_counts[static_cast<size_t>(c0 + i) * E + e] = run;
+        run += v[i];
+      }
     }
     counts[e] = run;
     rows += run;

@@ -32,7 +32,7 @@ __device__ __forceinline__ void warp_argmax(float& key, int& idx) {
 }
 
 template <int KPL>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+__global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                                     int T, int E, int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ wts) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -142,11 +142,12 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* wts,
                          cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const int blocks = (T + 7) / 8;
+  // one warp per block: the double-precision sigmoids of a few tokens spread over many SMs
+  const int blocks = T;
   const int kpl = (E + 31) / 32;
 #define KMOE_ROUTE(N)                                                             \
   if (kpl <= N) {                                                                 \
-    route_kernel<N><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, ids, wts);     \
+    route_kernel<N><<<blocks, 32, 0, st>>>(logits, bias, T, E, k, ids, wts);      \
     return cudaGetLastError();                                                    \
   }
   KMOE_ROUTE(1)
