@@ -26,36 +26,41 @@
 //               chunks NGRP*i + g of the tile
 //   last warp   TMA producer of the token rows and their scales (one lane)
 // Two producer warps keep more bulk copies in flight than one thread can.
-// Pipelines: STAGES smem stages (full/empty mbarriers) and two TMEM
-// accumulator buffers (acc_full/acc_empty) so the epilogue of one work item
-// overlaps the main loop of the next.  Every wait is bounded.
+// Pipelines: STAGES smem stages (full/empty mbarriers) and NACC TMEM
+// accumulator sets (acc_full/acc_empty); with two, the epilogue of one work
+// item overlaps the main loop of the next.  Every wait is bounded.
 //
 // Work items: for expert e with nt_e = ceil(rows_e / BN) token tiles and MT
-// weight tiles, items MT*tile_start[e] .. MT*tile_start[e+1]-1 are ordered
-// weight-tile-major, so the token tiles sharing one weight tile run side by
-// side (their weight reads meet in L2).  CTA b takes items b, b+grid, ...
+// weight tiles taken NT at a time (NT = 2 for the 224-row prefill tiles: two
+// 128-row weight tiles share each token-tile load, cutting the bytes moved per
+// MMA by 39%; one accumulator set then, as two do not fit in TMEM), items
+// (MT/NT)*tile_start[e] .. are ordered weight-tile-major, so the token tiles
+// sharing weight tiles run side by side (their weight reads meet in L2).
+// CTA b takes items b, b+grid, ...
 #include <cuda_fp8.h>
 
 #include "gemm.cuh"
 
 namespace kmoe {
 
-template <int BN_, int KPS_, int STAGES_, bool FC1_, int EPI_WARPS_ = 8, int CTAS_PER_SM_ = 1>
+template <int BN_, int KPS_, int STAGES_, bool FC1_, int EPI_WARPS_ = 8, int CTAS_PER_SM_ = 1, int NT_ = 1>
 struct GemmCfg {
   static constexpr int BN = BN_;
   static constexpr int KPS = KPS_;        // 128-wide K blocks per pipeline stage
   static constexpr int STAGES = STAGES_;
   static constexpr bool FC1 = FC1_;
   static constexpr int CTAS_PER_SM = CTAS_PER_SM_;
+  static constexpr int NT = NT_;          // 128-row weight tiles per work item (sharing the token tile)
+  static constexpr int NACC = NT == 1 ? 2 : 1;  // TMEM accumulator sets (2: epilogue overlaps next item)
   static constexpr int A_KB = 16384;     // 128 rows x 128 FP4 in the unpacked smem format
   static constexpr int A_TX_KB = 8192;   // transaction bytes of that tile (packed source)
   static constexpr int B_KB = BN * 128;  // token rows x 128 E4M3
   static constexpr int NCH = (BN + 127) / 128;
-  static constexpr int B_OFF = KPS * A_KB;
+  static constexpr int B_OFF = NT * KPS * A_KB;  // A: [tile][kbi][16 KB]
   static constexpr int SFA_OFF = B_OFF + KPS * B_KB;
-  static constexpr int SFB_OFF = SFA_OFF + KPS * 512;
+  static constexpr int SFB_OFF = SFA_OFF + NT * KPS * 512;
   static constexpr int STAGE = (SFB_OFF + KPS * NCH * 512 + 1023) / 1024 * 1024;
-  static constexpr int SFW = 4 + 4 * NCH;  // TMEM scale columns per K block (A, then B chunks)
+  static constexpr int SFW = 4 * NT + 4 * NCH;  // TMEM scale columns per K block (A tiles, then B chunks)
   static_assert(KPS * SFW <= 16, "scale columns per stage");
   static constexpr int EPI_WARPS = EPI_WARPS_;  // a multiple of 4 (one warp per TMEM lane quarter)
   static constexpr int NGRP = EPI_WARPS / 4;      // epilogue groups (column-chunk interleave)
@@ -65,8 +70,8 @@ struct GemmCfg {
   static constexpr int STG_BYTES = FC1 ? NGRP * STG_FLOATS * 4 : 0;
   static constexpr int BAR_OFF = STAGES * STAGE + STG_BYTES;
   static constexpr int SMEM = 1024 + BAR_OFF + 256;
-  static constexpr int SF_COL0 = 2 * BN;
-  static constexpr int TMEM_NEED = 2 * BN + STAGES * 16;
+  static constexpr int SF_COL0 = NACC * NT * BN;
+  static constexpr int TMEM_NEED = SF_COL0 + STAGES * 16;
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static_assert(BN % 32 == 0 && BN <= 256, "token tile must be a multiple of 32 rows, at most 256");
@@ -77,18 +82,20 @@ struct GemmCfg {
 };
 
 struct Work {
-  int e, m, tile, r0, n;
+  int e, m, tile, r0, n;  // m: weight-tile group (tiles NT*m + j)
 };
 
-__device__ __forceinline__ void decode_work(const GemmArgs& a, int BN, int w, Work& wk) {
-  int lo = 0, hi = a.E;  // largest e with MT*tile_start[e] <= w
+// Item w -> expert, weight-tile group m (tiles NT*m .. NT*m+NT-1), token tile.
+__device__ __forceinline__ void decode_work(const GemmArgs& a, int BN, int NT, int w, Work& wk) {
+  const int MG = a.MT / NT;  // weight-tile groups per expert
+  int lo = 0, hi = a.E;      // largest e with MG*tile_start[e] <= w
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (a.MT * __ldg(a.tile_start + mid) <= w) lo = mid; else hi = mid;
+    if (MG * __ldg(a.tile_start + mid) <= w) lo = mid; else hi = mid;
   }
   const int ts = __ldg(a.tile_start + lo);
   const int nt = __ldg(a.tile_start + lo + 1) - ts;
-  const int local = w - a.MT * ts;
+  const int local = w - MG * ts;
   const int t = local % nt;
   wk.e = lo;
   wk.m = local / nt;
@@ -161,7 +168,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
       mbar_init(&full[s], 2);  // one arrival per producer warp
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NACC; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], C::EPI_WARPS);
     }
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = a.MT * __ldg(a.tile_start + a.E);
+  const int total = (a.MT / C::NT) * __ldg(a.tile_start + a.E);
   const uint64_t budget = a.budget_ns;
 
   if (warp == 0 || warp == C::PRODB_WARP) {
@@ -195,11 +202,10 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Work wk;
-        decode_work(a, C::BN, w, wk);
+        decode_work(a, C::BN, C::NT, w, wk);
         const int ng = (wk.n + 31) >> 5;  // 32-row groups of the token tile
-        const uint32_t tx = is_a ? C::KPS * (C::A_TX_KB + 512) : C::KPS * (ng * 4096 + C::NCH * 512);
-        const int blk0 = (wk.e * a.MT + wk.m) * a.KB;
-        const uint8_t* wsf = a.wsf + static_cast<size_t>(blk0) * 512;
+        const uint32_t tx = is_a ? C::NT * C::KPS * (C::A_TX_KB + 512) : C::KPS * (ng * 4096 + C::NCH * 512);
+        const int blk0 = (wk.e * a.MT + C::NT * wk.m) * a.KB;  // first block of the item's first tile
         const uint8_t* bsf = a.bsf + static_cast<size_t>(wk.tile) * a.KB * C::NCH * 512;
         for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
           const int s = it % C::STAGES;
@@ -211,8 +217,13 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
           uint8_t* st = smem + s * C::STAGE;
           mbar_arrive_expect_tx(&full[s], tx);
           if (is_a) {
-            tma_load_3d(st, &maps.a, &full[s], 0, 0, blk0 + kb, pol);
-            bulk_load(st + C::SFA_OFF, wsf + static_cast<size_t>(kb) * 512, C::KPS * 512, &full[s]);
+#pragma unroll
+            for (int j = 0; j < C::NT; ++j) {
+              const int blk = blk0 + j * a.KB + kb;
+              tma_load_3d(st + j * C::KPS * C::A_KB, &maps.a, &full[s], 0, 0, blk, pol);
+              bulk_load(st + C::SFA_OFF + j * C::KPS * 512, a.wsf + static_cast<size_t>(blk) * 512, C::KPS * 512,
+                        &full[s]);
+            }
           } else {
 #pragma unroll
             for (int kbi = 0; kbi < C::KPS; ++kbi) {
@@ -250,12 +261,12 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++li) {
         Work wk;
-        decode_work(a, C::BN, w, wk);
-        const uint32_t acc = li & 1u;
-        const uint32_t aph = (li >> 1) & 1u;
+        decode_work(a, C::BN, C::NT, w, wk);
+        const uint32_t acc = li % C::NACC;
+        const uint32_t aph = (li / C::NACC) & 1u;
         if (!mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = tmem + acc * C::BN;
+        const uint32_t d = tmem + acc * C::NT * C::BN;  // tile j accumulates at d + j*BN
         const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
         const int nch = (wk.n + 127) >> 7;
         for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
@@ -270,17 +281,23 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
 #pragma unroll
           for (int kbi = 0; kbi < C::KPS; ++kbi) {
             const uint32_t sfc = tmem + C::SF_COL0 + s * 16 + kbi * C::SFW;
-            tc_cp_32x128b_warpx4(sfc, sdesc_sf_32x16(smem_u32(st + C::SFA_OFF + kbi * 512)));
+            const uint32_t sfb = sfc + 4 * C::NT;
+#pragma unroll
+            for (int j = 0; j < C::NT; ++j)
+              tc_cp_32x128b_warpx4(sfc + 4 * j, sdesc_sf_32x16(smem_u32(st + C::SFA_OFF + (j * C::KPS + kbi) * 512)));
             for (int c = 0; c < nch; ++c)
-              tc_cp_32x128b_warpx4(sfc + 4 + 4 * c,
+              tc_cp_32x128b_warpx4(sfb + 4 * c,
                                    sdesc_sf_32x16(smem_u32(st + C::SFB_OFF + (kbi * C::NCH + c) * 512)));
-            const uint32_t aaddr = smem_u32(st + kbi * C::A_KB);
             const uint32_t baddr = smem_u32(st + C::B_OFF + kbi * C::B_KB);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              mma_mxf8f6f4(d, sdesc_kmajor_sw128(aaddr + 32 * kk), sdesc_kmajor_sw128(baddr + 32 * kk),
-                           idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, kk, kk), sfc, sfc + 4,
-                           (kb | kbi | kk) != 0);
+            for (int j = 0; j < C::NT; ++j) {
+              const uint32_t aaddr = smem_u32(st + (j * C::KPS + kbi) * C::A_KB);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                mma_mxf8f6f4(d + j * C::BN, sdesc_kmajor_sw128(aaddr + 32 * kk), sdesc_kmajor_sw128(baddr + 32 * kk),
+                             idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, kk, kk), sfc + 4 * j, sfb,
+                             (kb | kbi | kk) != 0);
+              }
             }
           }
           tc_commit(&empty[s]);
@@ -301,20 +318,25 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
     uint32_t li = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++li) {
       Work wk;
-      decode_work(a, C::BN, w, wk);
-      const uint32_t acc = li & 1u;
-      const uint32_t aph = (li >> 1) & 1u;
+      decode_work(a, C::BN, C::NT, w, wk);
+      const uint32_t acc = li % C::NACC;
+      const uint32_t aph = (li / C::NACC) & 1u;
       bool ok = mbar_wait_bounded(&acc_full[acc], aph, budget, a.err, abort_flag);
       ok = named_barrier_and(1, 32 * C::EPI_WARPS, ok && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::BN;
-      for (int c0 = 32 * grp; c0 < wk.n; c0 += 32 * C::NGRP) {
+      // chunks of 32 columns of the NT accumulators, round-robin over the groups
+      const int nchunk = (wk.n + 31) >> 5;
+      for (int ci = grp; ci < C::NT * nchunk; ci += C::NGRP) {
+        const int j = ci / nchunk;             // weight tile of the item
+        const int c0 = (ci - j * nchunk) * 32;  // first column of the chunk
+        const int mt = C::NT * wk.m + j;        // weight tile index within the expert
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + (acc * C::NT + j) * C::BN;
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c0, r);
         tmem_ld_wait();
         if (!C::FC1) {
-          const int h = 128 * wk.m + 32 * q + lane;
+          const int h = 128 * mt + 32 * q + lane;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int col = c0 + jj;
@@ -359,11 +381,10 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
               w[k4] = (lo & 0xFFFFu) | (hi << 16);
             }
             if (col < wk.n) {
-              *reinterpret_cast<uint4*>(a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * wk.m + i0) =
+              *reinterpret_cast<uint4*>(a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0) =
                   make_uint4(w[0], w[1], w[2], w[3]);
               if (hh == 0)
-                a.isf[tile_sf_offset(wk.tile, col, 2 * wk.m + gh, C::NCH, a.I / 128)] =
-                    static_cast<uint8_t>(e + 127);
+                a.isf[tile_sf_offset(wk.tile, col, 2 * mt + gh, C::NCH, a.I / 128)] = static_cast<uint8_t>(e + 127);
             }
           }
           named_barrier(2 + grp, 128);
@@ -460,13 +481,17 @@ cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, con
                                   : launch_one<GemmCfg<32, 1, 8, true>>(maps, a, grid, st);
     if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 3, true>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<64, 1, 6, true>>(maps, a, grid, st);
-    if (BN == 224 && kps == 1) return launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
+    if (BN == 224 && kps == 1)
+      return a.MT % 2 == 0 ? launch_one<GemmCfg<224, 1, 3, true, 8, 1, 2>>(maps, a, grid, st)
+                           : launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
   } else {
     if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<32, 1, 8, false>>(maps, a, grid, st);
     if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 4, false>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<64, 1, 7, false>>(maps, a, grid, st);
-    if (BN == 224 && kps == 1) return launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st);
+    if (BN == 224 && kps == 1)
+      return a.MT % 2 == 0 ? launch_one<GemmCfg<224, 1, 3, false, 8, 1, 2>>(maps, a, grid, st)
+                           : launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st);
   }
   return cudaErrorInvalidValue;
 }
