@@ -6,10 +6,12 @@
 // One warp per token.  Lane l holds the keys of experts l, l+32, l+64, ...
 // The selection key is fp32(sigmoid(logit)) + fp32(bias) with the sigmoid
 // correctly rounded to fp32 (evaluated in double).  Double precision is slow
-// on this part, so a first pass ranks cheap fp32 keys, and only experts whose
-// cheap key lies within a safety margin of the k-th largest (the margin is
-// far above the error of expf) get the exact key; the final top-k is taken
-// over exact keys, equal keys going to the lower expert index.
+// on this part, so a radix select first finds the k-th largest cheap fp32
+// key, and only experts whose cheap key lies within a safety margin of it
+// (the margin is far above the error of expf) get the exact key; the final
+// top-k is taken over exact keys, equal keys going to the lower expert index.
+// Usually the candidates fit one per lane and are ranked in one pass; with
+// more than 32 (many equal keys) k rounds of warp arg-max are used instead.
 #include "common.cuh"
 
 namespace kmoe {
@@ -51,27 +53,74 @@ __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ log
     float kf = s + b[i];
     key[i] = (e < E && !isnan(kf)) ? kf : NEG_INF;
   }
-  // pass 1: k-th largest cheap key
-  uint32_t taken = 0;
-  float kth = NEG_INF;
-  for (int j = 0; j < k; ++j) {
-    float bk = NEG_INF;
-    int bi = 0x7fffffff;
+  // pass 1: the k-th largest cheap key, by a bitwise radix select over
+  // order-preserving integer images of the keys (32 counting rounds)
+  uint32_t okey[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const uint32_t u = __float_as_uint(key[i]);
+    okey[i] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  uint32_t prefix = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t probe = prefix | (1u << bit);
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) cnt += (lane + 32 * i < E && okey[i] >= probe) ? 1 : 0;
+    if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt))) >= k) prefix = probe;
+  }
+  const float kth = __uint_as_float((prefix & 0x80000000u) ? (prefix & 0x7fffffffu) : ~prefix);
+
+  // fast path: gather the candidates (cheap key within the margin of the k-th)
+  // into one lane each, take their exact keys and rank them across the warp
+  {
+    const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
+    const float cut = (kth == NEG_INF) ? NEG_INF : kth - margin;
+    __shared__ int s_idx[32];
+    __shared__ float s_lg[32], s_b[32];
+    int base = 0;
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && e < bi))) {
-        bk = key[i];
-        bi = e;
+      const bool pred = e < E && key[i] >= cut;
+      const unsigned m = __ballot_sync(0xffffffffu, pred);
+      const int pos = base + __popc(m & ((1u << lane) - 1u));
+      if (pred && pos < 32) {
+        s_idx[pos] = e;
+        s_lg[pos] = lgt[i];
+        s_b[pos] = b[i];
       }
+      base += __popc(m);
     }
-    warp_argmax(bk, bi);
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    kth = bk;
+    __syncwarp();
+    if (base <= 32) {
+      const bool have = lane < base;
+      const int idx = have ? s_idx[lane] : 0x7fffffff;
+      const float sv = have ? sigmoid_exact_f32(s_lg[lane]) : 0.f;
+      float kx = have ? sv + s_b[lane] : NEG_INF;
+      if (isnan(kx)) kx = NEG_INF;
+      int rank = 0;
+      for (int j = 0; j < 32; ++j) {
+        const float kj = __shfl_sync(0xffffffffu, kx, j);
+        const int ij = __shfl_sync(0xffffffffu, idx, j);
+        rank += (kj > kx || (kj == kx && ij < idx)) ? 1 : 0;
+      }
+      const bool sel = have && rank < k;
+      double sum = sel ? static_cast<double>(sv) : 0.0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (sel) {
+        ids[static_cast<size_t>(warp) * k + rank] = idx;
+        wts[static_cast<size_t>(warp) * k + rank] = static_cast<float>(static_cast<double>(sv) / sum);
+      }
+      return;
+    }
   }
-  // pass 2: exact keys for the candidates.  Each lane evaluates one candidate
-  // per round (all lanes in step), so the double-precision work per warp is
-  // the largest candidate count of any lane rather than the candidate total.
+  // general path (more than 32 candidates, e.g. many equal keys): k rounds of
+  // warp arg-max over the exact keys of all candidates
+  uint32_t taken = 0;
+  // exact keys for the candidates: each lane evaluates one candidate per
+  // round (all lanes in step)
   const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
   const float cut = (kth == NEG_INF) ? NEG_INF : kth - margin;
   uint32_t cand = 0;
@@ -106,7 +155,6 @@ __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ log
 #pragma unroll
   for (int i = 0; i < KPL; ++i)
     if (!((cand0 >> i) & 1u)) key[i] = NEG_INF;  // not a candidate: cannot be chosen
-  taken = 0;
   float mys = 0.f;
   int myid = -1;
   double sum = 0.0;
