@@ -68,6 +68,13 @@ def barrier(dist):
         dist.barrier()
 
 
+def job_throughput(dist, world_size, tokens_per_rank_step, steps, rank_ms, device):
+    """Whole-job tokens/s: the tokens of all ranks over the slowest rank's time
+    (every rank runs its own replica of the layer; no data-path collective)."""
+    slowest_ms = reduce_max(dist, rank_ms, device)
+    return world_size * tokens_per_rank_step * steps / (slowest_ms / 1e3), slowest_ms
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples during the timed region (200 ms period)."""
@@ -333,9 +340,8 @@ def run_ours(args):
     layer = Layer(wp, device)
     clocks = ClockSampler(local) if rank == 0 else None
     total_ms, clk = time_layer(layer, args.steps, args.warmup, dist, device, clocks)
-    total_ms = reduce_max(dist, total_ms, device)
+    tokens_s, total_ms = job_throughput(dist, ws, wp.T, args.steps, total_ms, device)
     ms_step = total_ms / args.steps
-    tokens_s = ws * wp.T * args.steps / (total_ms / 1e3)
     tflops = wp.flops() / (ms_step / 1e3) / 1e12
     stages = time_stages(layer, max(3, min(args.steps, 10)))
     layer.check()
@@ -345,8 +351,7 @@ def run_ours(args):
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
     traffic = fc1_traffic_record()
     e2e_ms, h2d, d2h = e2e_time(layer, args.steps, max(1, args.warmup // 2))
-    e2e_ms = reduce_max(dist, e2e_ms, device)
-    e2e_tok_s = ws * wp.T * args.steps / (e2e_ms / 1e3)
+    e2e_tok_s, e2e_ms = job_throughput(dist, ws, wp.T, args.steps, e2e_ms, device)
     touched_p = layer.touched_experts()
     weights = layer.weights
     del layer
