@@ -231,6 +231,29 @@ def time_stages(layer, steps):
     return (acc / steps).tolist()
 
 
+def mma_peak(device, N=224, iters=500000):
+    """Measured tensor-pipe roof of the GEMMs' instruction (kmoe_mma_peak_run):
+    block-scaled E2M1 x E4M3 MMAs on resident operands, one CTA per SM."""
+    import torch
+    import mxfp8_mxfp4_moe_gb300 as K
+    ws = torch.zeros(256, dtype=torch.uint8, device=device)
+    K.kmoe_mma_peak_run(1000, N, ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    flops = K.kmoe_mma_peak_run(iters, N, ws)
+    e.record()
+    torch.cuda.synchronize()
+    st, word = K.kmoe_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"peak kernel device error {word:#x}")
+    ms = s.elapsed_time(e)
+    return {"tflops": flops / (ms / 1e3) / 1e12, "N": N, "duration_ms": ms,
+            "what": "tcgen05.mma kind::mxf8f6f4 block-scaled E2M1 x E4M3, M=128, operands resident in smem, "
+                    "one CTA per SM"}
+
+
 def e2e_time(layer, steps, warmup):
     """Same metric through the C ABI with host buffers: per step the H2D copy of
     x, logits and bias from pinned memory, the forward, and the D2H read of the
@@ -372,6 +395,8 @@ def run_ours(args):
     d_layer_bytes = touched * per_expert_all + 2 * wd.T * wd.H * 2 + 4 * wd.T * wd.E
     d_layer_gbs = d_layer_bytes / (d_us / 1e6) / 1e9
 
+    peak_mma = mma_peak(device)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tps, ntok, secs, cores = oracle_sample(wp, budget_s=args.cpu_budget_s)
@@ -397,7 +422,9 @@ def run_ours(args):
                          "achieved": fc1_tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": fc1_tf / fp8_peak,
                          "peak_source": f"{peaks_kind}: 2 x bf16_tflops_sustained (nominal FP8/BF16 ratio 2)",
                          "algorithmic": f"4*R*H*I = {fc1_flops:.4g} FLOP per launch",
-                         "traffic": (traffic["dram_bytes_per_launch"] if traffic else None)},
+                         "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
+                         "frac_of_measured_mma_roof": fc1_tf / peak_mma["tflops"]},
+            "mma_peak_measured": peak_mma,
             "decode": {"workload": "Kimi-K3 MoE layer decode T=16 H=7168 I=3584 E=896 top-16",
                        "us_per_layer": d_us, "touched_experts": touched, "layer_GBs": d_layer_gbs,
                        "layer_hbm_frac": d_layer_gbs / peaks["hbm_gbs"],

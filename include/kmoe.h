@@ -202,6 +202,16 @@ int kmoe_device_error(void* workspace, uint32_t* word, cudaStream_t stream);
  * tile capacity of the array.  Host helper for inspection. */
 size_t kmoe_tile_sf_offset(int tile, int local_row, int g, int tile_rows, int K, int max_tiles);
 
+/* Measurement aid: the tensor-pipe roof of the instruction the expert GEMMs
+ * issue (tcgen05.mma .kind::mxf8f6f4 block-scaled, E2M1 A of 128 rows x E4M3
+ * B of N rows, K = 32 per instruction).  Launches one CTA per SM, each issuing
+ * 4 * iters such instructions on operands resident in shared memory; the
+ * caller times the stream.  FLOPs of the launch:
+ * num_SMs * iters * 4 * 2 * 128 * N * 32.  N a multiple of 16 in [16, 256],
+ * iters in [1, 2^24].  A wait that gives up sets the timeout bit of
+ * workspace's error word (read with kmoe_device_error). */
+int kmoe_mma_peak_run(int iters, int N, void* workspace, cudaStream_t stream);
+
 /* Self-test of the bounded device wait: launches one block that waits on a
  * barrier nobody arrives at, for at most `budget_us` microseconds, and
  * reports the outcome in workspace's error word (read it with

@@ -26,7 +26,7 @@ KMOE_MXFP4_E2M1 = 1
 EXPORTS = ("kmoe_status_string", "kmoe_check_device", "kmoe_workspace_size", "kmoe_workspace_layout",
            "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_weight_bytes", "kmoe_prepare_weights",
            "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error", "kmoe_tile_sf_offset",
-           "kmoe_selftest_wait_timeout", "kmoe_forward_noalloc")
+           "kmoe_selftest_wait_timeout", "kmoe_forward_noalloc", "kmoe_mma_peak_run")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -82,6 +82,8 @@ def load_library(path: str = LIB_PATH):
     lib.kmoe_tile_sf_offset.restype = S
     lib.kmoe_tile_sf_offset.argtypes = [I, I, I, I, I, I]
     lib.kmoe_selftest_wait_timeout.argtypes = [P, I, V]
+    lib.kmoe_mma_peak_run.argtypes = [I, I, P, V]
+    lib.kmoe_mma_peak_run.restype = ctypes.c_int
     lib.kmoe_forward_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, V]
     lib.kmoe_forward_noalloc.restype = ctypes.c_int
     for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
@@ -238,6 +240,13 @@ def kmoe_device_error(workspace, stream=None):
 
 def kmoe_tile_sf_offset(tile, local_row, g, tile_rows, K, max_tiles):
     return _lib.kmoe_tile_sf_offset(tile, local_row, g, tile_rows, K, max_tiles)
+
+
+def kmoe_mma_peak_run(iters, N, workspace, stream=None):
+    """Launch the tensor-pipe roof kernel; returns the launch's FLOP count."""
+    _check("kmoe_mma_peak_run", _lib.kmoe_mma_peak_run(iters, N, _ptr(workspace), _stream(stream)))
+    sms = torch.cuda.get_device_properties(workspace.device).multi_processor_count
+    return sms * iters * 4 * 2 * 128 * N * 32
 
 
 def kmoe_selftest_wait_timeout(workspace, budget_us, stream=None):

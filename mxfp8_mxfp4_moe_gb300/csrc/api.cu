@@ -20,6 +20,7 @@ cudaError_t launch_quant_scatter(const void*, int, int, int, int, int, int, int,
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int, int, int, int, float, void*,
                            cudaStream_t);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t budget_ns, cudaStream_t st);
+cudaError_t launch_mma_peak(int iters, int N, int grid, uint32_t* err, cudaStream_t st);
 __global__ void kmoe_probe_kernel();
 }  // namespace kmoe
 
@@ -315,6 +316,14 @@ int kmoe_device_error(void* workspace, uint32_t* word, cudaStream_t stream) {
   if (word) *word = v;
   if (v & KMOE_DEVERR_TIMEOUT) return KMOE_ERR_TIMEOUT;
   if (v) return KMOE_ERR_DEVICE;
+  return KMOE_OK;
+}
+
+int kmoe_mma_peak_run(int iters, int N, void* workspace, cudaStream_t stream) {
+  if (!workspace || iters < 1 || iters > (1 << 24) || N < 16 || N > 256 || N % 16 != 0) return KMOE_ERR_ARG;
+  const int grid = num_sms();
+  if (grid <= 0) return KMOE_ERR_CUDA;
+  KMOE_CK(launch_mma_peak(iters, N, grid, static_cast<uint32_t*>(workspace), stream));
   return KMOE_OK;
 }
 

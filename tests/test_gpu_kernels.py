@@ -110,3 +110,14 @@ def test_bounded_wait_timeout_keeps_context(K):
     # the context still works
     ids, _ = K.kmoe_route(torch.zeros(2, 8, device="cuda"), torch.zeros(8, device="cuda"), 2)
     assert ids.cpu().tolist() == [[0, 1], [0, 1]]
+
+
+def test_mma_peak_kernel_runs(K):
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    flops = K.kmoe_mma_peak_run(2000, 224, ws)
+    torch.cuda.synchronize()
+    st, word = K.kmoe_device_error(ws)
+    assert st == 0 and word == 0
+    assert flops == torch.cuda.get_device_properties(0).multi_processor_count * 2000 * 4 * 2 * 128 * 224 * 32
+    with pytest.raises(K.KmoeError):
+        K.kmoe_mma_peak_run(10, 200, ws)   # N not a multiple of 16
