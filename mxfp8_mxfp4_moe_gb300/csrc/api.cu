@@ -265,8 +265,9 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   if (!make_weight_map(&m1.a, w13_k, weight_blocks(p, 0), kps1) ||
       !make_weight_map(&m2.a, w2_k, weight_blocks(p, 1), kps2))
     return KMOE_ERR_CUDA;
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t rows = i < 3 ? (32u << i) : static_cast<uint32_t>(L.BN);  // 32, 64, 128 rows, one tile
+  for (int i = 0; i < 5; ++i) {
+    // 32, 64, 128 rows, one tile, half a tile
+    const uint32_t rows = i < 3 ? (32u << i) : static_cast<uint32_t>(i == 3 ? L.BN : L.BN / 2);
     if (!make_map(&m1.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, H, R, H, 128, rows) ||
         !make_map(&m2.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, iq, I, R, I, 128, rows))
       return KMOE_ERR_CUDA;

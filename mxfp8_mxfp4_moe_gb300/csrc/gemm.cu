@@ -37,9 +37,7 @@
 // (MT/NT)*tile_start[e] .. are ordered weight-tile-major, so the token tiles
 // sharing weight tiles run side by side (their weight reads meet in L2).
 // CTA b takes items b, b+grid, ...
-#include <cuda_fp8.h>
-
-#include "gemm.cuh"
+#include "gemm_dev.cuh"
 
 namespace kmoe {
 
@@ -69,7 +67,8 @@ struct GemmCfg {
   static constexpr int STG_FLOATS = 128 * 33;  // one 128 x 32 staging tile (padded rows) per group
   static constexpr int STG_BYTES = FC1 ? NGRP * STG_FLOATS * 4 : 0;
   static constexpr int BAR_OFF = STAGES * STAGE + STG_BYTES;
-  static constexpr int SMEM = 1024 + BAR_OFF + 256;
+  static constexpr int TS_OFF = BAR_OFF + 256;  // shared copy of tile_start
+  static constexpr int SMEM = 1024 + TS_OFF + kTileStartBytes;
   static constexpr int SF_COL0 = NACC * NT * BN;
   static constexpr int TMEM_NEED = SF_COL0 + STAGES * 16;
   static constexpr int TMEM_COLS =
@@ -80,73 +79,6 @@ struct GemmCfg {
   static_assert(TMEM_COLS * CTAS_PER_SM <= 512, "TMEM budget per SM");
   static_assert(EPI_WARPS % 4 == 0, "epilogue warps cover the four lane quarters");
 };
-
-struct Work {
-  int e, m, tile, r0, n;  // m: weight-tile group (tiles NT*m + j)
-};
-
-// Item w -> expert, weight-tile group m (tiles NT*m .. NT*m+NT-1), token tile.
-__device__ __forceinline__ void decode_work(const GemmArgs& a, int BN, int NT, int w, Work& wk) {
-  const int MG = a.MT / NT;  // weight-tile groups per expert
-  int lo = 0, hi = a.E;      // largest e with MG*tile_start[e] <= w
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (MG * __ldg(a.tile_start + mid) <= w) lo = mid; else hi = mid;
-  }
-  const int ts = __ldg(a.tile_start + lo);
-  const int nt = __ldg(a.tile_start + lo + 1) - ts;
-  const int local = w - MG * ts;
-  const int t = local % nt;
-  wk.e = lo;
-  wk.m = local / nt;
-  wk.tile = ts + t;
-  wk.r0 = __ldg(a.seg_start + lo) + t * BN;
-  const int left = __ldg(a.counts + lo) - t * BN;
-  wk.n = left < BN ? left : BN;
-}
-
-__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(out)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-      : "memory");
-  return out != 0;
-}
-
-// 1 - exp(-x) and exp(-x) for x >= 0: a Taylor polynomial below 1/4 (no
-// cancellation; truncation error x^8/8! < 4e-10 relative), 1 - q above.
-__device__ __forceinline__ void one_minus_exp_neg(float x, float& om, float& q) {
-  q = __expf(-x);
-  float p = 1.0f / 5040.0f;
-  p = fmaf(p, x, -1.0f / 720.0f);
-  p = fmaf(p, x, 1.0f / 120.0f);
-  p = fmaf(p, x, -1.0f / 24.0f);
-  p = fmaf(p, x, 1.0f / 6.0f);
-  p = fmaf(p, x, -0.5f);
-  p = fmaf(p, x, 1.0f);
-  om = x < 0.25f ? x * p : 1.0f - q;
-}
-
-// SiTU(g, u) = beta*tanh(g/beta)*sigmoid(g) * beta_lin*tanh(u/beta_lin) in fp32
-// from exponentials of non-positive arguments only:
-//   tanh(|v|/b) = (1 - q)/(1 + q),  q = exp(-2|v|/b)
-//   sigmoid(g) = 1/(1 + r) (g >= 0) or r/(1 + r) (g < 0),  r = exp(-|g|)
-// so the product is one quotient: no cancellation, no overflow, a few ulp.
-// kg = 2/beta, ku = 2/beta_lin, bb = beta*beta_lin.
-__device__ __forceinline__ float situ_f32(float g, float u, float kg, float ku, float bb) {
-  const float ag = fabsf(g), au = fabsf(u);
-  float omg, qg, omu, qu;
-  one_minus_exp_neg(ag * kg, omg, qg);
-  one_minus_exp_neg(au * ku, omu, qu);
-  const float r = __expf(-ag);
-  const float num = (omg * omu) * (g >= 0.0f ? 1.0f : r);
-  const float den = ((1.0f + qg) * (1.0f + qu)) * (1.0f + r);
-  const float mag = bb * __fdividef(num, den);
-  return ((g < 0.0f) != (u < 0.0f)) ? -mag : mag;
-}
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(const __grid_constant__ GemmMaps maps,
@@ -160,6 +92,8 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
   uint64_t* done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* tsm = reinterpret_cast<int32_t*>(smem + C::TS_OFF);
+  stage_tile_start(a, tsm);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -188,7 +122,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = (a.MT / C::NT) * __ldg(a.tile_start + a.E);
+  const int total = (a.MT / C::NT) * tsm[a.E];
   const uint64_t budget = a.budget_ns;
 
   if (warp == 0 || warp == C::PRODB_WARP) {
@@ -202,7 +136,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Work wk;
-        decode_work(a, C::BN, C::NT, w, wk);
+        decode_work(a, tsm, C::BN, C::NT, w, wk);
         const int ng = (wk.n + 31) >> 5;  // 32-row groups of the token tile
         const uint32_t tx = is_a ? C::NT * C::KPS * (C::A_TX_KB + 512) : C::KPS * (ng * 4096 + C::NCH * 512);
         const int blk0 = (wk.e * a.MT + C::NT * wk.m) * a.KB;  // first block of the item's first tile
@@ -256,51 +190,62 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Lean issue loop (the tensor pipe takes the next MMA only about as fast
+    // as it runs one): descriptors are formed once and advanced by adds (the
+    // start-address field holds smem offset >> 4).
     if (lane == 0) {
-      uint32_t it = 0, li = 0;
+      constexpr uint32_t kStageD = C::STAGE >> 4;
+      const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
+      const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + C::B_OFF));
+      const uint64_t sfadesc0 = sdesc_sf_32x16(smem_u32(smem + C::SFA_OFF));
+      const uint64_t sfbdesc0 = sdesc_sf_32x16(smem_u32(smem + C::SFB_OFF));
+      int s = 0;
+      uint32_t ph = 0, li = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++li) {
         Work wk;
-        decode_work(a, C::BN, C::NT, w, wk);
+        decode_work(a, tsm, C::BN, C::NT, w, wk);
         const uint32_t acc = li % C::NACC;
         const uint32_t aph = (li / C::NACC) & 1u;
         if (!mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * C::NT * C::BN;  // tile j accumulates at d + j*BN
         const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
-        const int nch = (wk.n + 127) >> 7;
-        for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1u;
+        const int nch = static_cast<int>((nmma + 127u) >> 7);
+        uint32_t idk[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) idk[kk] = idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, kk, kk);
+        for (int kb = 0; kb < a.KB; kb += C::KPS) {
           if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          uint8_t* st = smem + s * C::STAGE;
+          const uint64_t so = static_cast<uint64_t>(s) * kStageD;
+          const uint32_t sf0 = tmem + C::SF_COL0 + static_cast<uint32_t>(s) * 16;
 #pragma unroll
           for (int kbi = 0; kbi < C::KPS; ++kbi) {
-            const uint32_t sfc = tmem + C::SF_COL0 + s * 16 + kbi * C::SFW;
+            const uint32_t sfc = sf0 + kbi * C::SFW;
             const uint32_t sfb = sfc + 4 * C::NT;
 #pragma unroll
-            for (int j = 0; j < C::NT; ++j)
-              tc_cp_32x128b_warpx4(sfc + 4 * j, sdesc_sf_32x16(smem_u32(st + C::SFA_OFF + (j * C::KPS + kbi) * 512)));
-            for (int c = 0; c < nch; ++c)
-              tc_cp_32x128b_warpx4(sfb + 4 * c,
-                                   sdesc_sf_32x16(smem_u32(st + C::SFB_OFF + (kbi * C::NCH + c) * 512)));
-            const uint32_t baddr = smem_u32(st + C::B_OFF + kbi * C::B_KB);
+            for (int j = 0; j < C::NT; ++j) tc_cp_32x128b_warpx4(sfc + 4 * j, sfadesc0 + so + (j * C::KPS + kbi) * 32);
+            tc_cp_32x128b_warpx4(sfb, sfbdesc0 + so + kbi * C::NCH * 32);
+            if (C::NCH > 1 && nch > 1) tc_cp_32x128b_warpx4(sfb + 4, sfbdesc0 + so + kbi * C::NCH * 32 + 32);
+            const uint64_t bd = bdesc0 + so + kbi * (C::B_KB >> 4);
 #pragma unroll
             for (int j = 0; j < C::NT; ++j) {
-              const uint32_t aaddr = smem_u32(st + (j * C::KPS + kbi) * C::A_KB);
+              const uint64_t ad = adesc0 + so + (j * C::KPS + kbi) * (C::A_KB >> 4);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                mma_mxf8f6f4(d + j * C::BN, sdesc_kmajor_sw128(aaddr + 32 * kk), sdesc_kmajor_sw128(baddr + 32 * kk),
-                             idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, kk, kk), sfc + 4 * j, sfb,
+              for (int kk = 0; kk < 4; ++kk)
+                mma_mxf8f6f4(d + j * C::BN, ad + 2 * kk, bd + 2 * kk, idk[kk], sfc + 4 * j, sfb,
                              (kb | kbi | kk) != 0);
-              }
             }
           }
           tc_commit(&empty[s]);
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
         tc_commit(&acc_full[acc]);
@@ -318,7 +263,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
     uint32_t li = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++li) {
       Work wk;
-      decode_work(a, C::BN, C::NT, w, wk);
+      decode_work(a, tsm, C::BN, C::NT, w, wk);
       const uint32_t acc = li % C::NACC;
       const uint32_t aph = (li / C::NACC) & 1u;
       bool ok = mbar_wait_bounded(&acc_full[acc], aph, budget, a.err, abort_flag);
@@ -332,63 +277,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
         const int c0 = (ci - j * nchunk) * 32;  // first column of the chunk
         const int mt = C::NT * wk.m + j;        // weight tile index within the expert
         const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + (acc * C::NT + j) * C::BN;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c0, r);
-        tmem_ld_wait();
-        if (!C::FC1) {
-          const int h = 128 * mt + 32 * q + lane;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int col = c0 + jj;
-            if (col < wk.n) {
-              const int slot = __ldg(a.slot_of_row + wk.r0 + col);
-              a.y[static_cast<size_t>(slot) * a.H + h] = __uint_as_float(r[jj]);
-            }
-          }
-        } else {
-          float* row = stg + (32 * q + lane) * 33;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) row[jj] = __uint_as_float(r[jj]);
-          named_barrier(2 + grp, 128);
-          {
-            // thread -> (column, 32-group of the 64 intermediate indices, half):
-            // 16 consecutive intermediate values of one token row per thread
-            const int t = eq * 32 + lane;
-            const int cl = t >> 2;
-            const int gh = (t >> 1) & 1;
-            const int hh = t & 1;
-            const int col = c0 + cl;
-            const int i0 = 32 * gh + 16 * hh;
-            float act[16];
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g = stg[(i0 + i) * 33 + cl];
-              const float u = stg[(64 + i0 + i) * 33 + cl];
-              act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
-              amax = fmaxf(amax, fabsf(act[i]));
-            }
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the other half of the group
-            const int e = e4m3_scale_exp(amax);
-            const float inv = exp2i(-e);
-            uint32_t w[4];
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4] * inv, act[4 * k4 + 1] * inv),
-                                                           __NV_SATFINITE, __NV_E4M3);
-              const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-                  make_float2(act[4 * k4 + 2] * inv, act[4 * k4 + 3] * inv), __NV_SATFINITE, __NV_E4M3);
-              w[k4] = (lo & 0xFFFFu) | (hi << 16);
-            }
-            if (col < wk.n) {
-              *reinterpret_cast<uint4*>(a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
-              if (hh == 0)
-                a.isf[tile_sf_offset(wk.tile, col, 2 * mt + gh, C::NCH, a.I / 128)] = static_cast<uint8_t>(e + 127);
-            }
-          }
-          named_barrier(2 + grp, 128);
-        }
+        epilogue_chunk<C::FC1, C::NCH>(a, wk, mt, tbase, c0, stg, q, eq, lane, grp);
       }
       tc_fence_before();
       __syncwarp();

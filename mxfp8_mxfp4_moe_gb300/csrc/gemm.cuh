@@ -9,10 +9,11 @@ namespace kmoe {
 constexpr int kWeightBlockBytes = 8192 + 512;
 
 // Tensor maps of one grouped GEMM: the weight codes (box of kps K blocks)
-// and the token rows in boxes of 32, 64, 128 rows and of one whole tile.
+// and the token rows in boxes of 32, 64, 128 rows, of one whole tile and of
+// half a tile (the share of one CTA of a pair).
 struct GemmMaps {
   CUtensorMap a;
-  CUtensorMap b[4];
+  CUtensorMap b[5];
 };
 
 // K blocks (of 128) moved per pipeline stage for a token-tile size and a K
@@ -48,5 +49,9 @@ cudaError_t launch_prep_weights(const uint8_t* codes, const uint8_t* sf, uint8_t
 // kps must equal gemm_kblocks_per_stage(BN, a.KB) (the depth of maps.a's box).
 cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, const GemmArgs& a, int grid,
                             cudaStream_t st);
+
+// The CTA-pair kernel for BN = 224 (gemm_pair.cu); a.MT must be even.  `sms`
+// is the SM count; the grid is the number of co-resident pairs.
+cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st);
 
 }  // namespace kmoe

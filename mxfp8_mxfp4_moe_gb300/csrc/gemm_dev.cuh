@@ -1,0 +1,158 @@
+// Device pieces shared by the one-CTA and the CTA-pair expert GEMM kernels:
+// work-item decoding, the SiTU activation and the epilogue of one 32-column
+// accumulator chunk.
+#pragma once
+#include <cuda_fp8.h>
+
+#include "gemm.cuh"
+
+namespace kmoe {
+
+struct Work {
+  int e, m, tile, r0, n;  // m: weight-tile group (tiles NT*m + j)
+};
+
+// Shared-memory bytes of the tile_start copy (E+1 <= kMaxE+1 ints).
+constexpr int kTileStartBytes = ((kMaxE + 1) * 4 + 255) / 256 * 256;
+
+// Copy tile_start[0..E] into shared memory; every thread of the CTA takes
+// part, before the CTA's first barrier.
+__device__ __forceinline__ void stage_tile_start(const GemmArgs& a, int32_t* ts) {
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) ts[i] = __ldg(a.tile_start + i);
+}
+
+// Item w -> expert, weight-tile group m (tiles NT*m .. NT*m+NT-1), token tile.
+// `tsm` is the shared-memory copy of tile_start.
+__device__ __forceinline__ void decode_work(const GemmArgs& a, const int32_t* tsm, int BN, int NT, int w, Work& wk) {
+  const int MG = a.MT / NT;  // weight-tile groups per expert
+  int lo = 0, hi = a.E;      // largest e with MG*tile_start[e] <= w
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (MG * tsm[mid] <= w) lo = mid; else hi = mid;
+  }
+  const int ts = tsm[lo];
+  const int nt = tsm[lo + 1] - ts;
+  const int local = w - MG * ts;
+  const int t = local % nt;
+  wk.e = lo;
+  wk.m = local / nt;
+  wk.tile = ts + t;
+  wk.r0 = __ldg(a.seg_start + lo) + t * BN;
+  const int left = __ldg(a.counts + lo) - t * BN;
+  wk.n = left < BN ? left : BN;
+}
+
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
+// 1 - exp(-x) and exp(-x) for x >= 0: a Taylor polynomial below 1/4 (no
+// cancellation; truncation error x^8/8! < 4e-10 relative), 1 - q above.
+__device__ __forceinline__ void one_minus_exp_neg(float x, float& om, float& q) {
+  q = __expf(-x);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, x, -1.0f / 720.0f);
+  p = fmaf(p, x, 1.0f / 120.0f);
+  p = fmaf(p, x, -1.0f / 24.0f);
+  p = fmaf(p, x, 1.0f / 6.0f);
+  p = fmaf(p, x, -0.5f);
+  p = fmaf(p, x, 1.0f);
+  om = x < 0.25f ? x * p : 1.0f - q;
+}
+
+// SiTU(g, u) = beta*tanh(g/beta)*sigmoid(g) * beta_lin*tanh(u/beta_lin) in fp32
+// from exponentials of non-positive arguments only:
+//   tanh(|v|/b) = (1 - q)/(1 + q),  q = exp(-2|v|/b)
+//   sigmoid(g) = 1/(1 + r) (g >= 0) or r/(1 + r) (g < 0),  r = exp(-|g|)
+// so the product is one quotient: no cancellation, no overflow, a few ulp.
+// kg = 2/beta, ku = 2/beta_lin, bb = beta*beta_lin.
+__device__ __forceinline__ float situ_f32(float g, float u, float kg, float ku, float bb) {
+  const float ag = fabsf(g), au = fabsf(u);
+  float omg, qg, omu, qu;
+  one_minus_exp_neg(ag * kg, omg, qg);
+  one_minus_exp_neg(au * ku, omu, qu);
+  const float r = __expf(-ag);
+  const float num = (omg * omu) * (g >= 0.0f ? 1.0f : r);
+  const float den = ((1.0f + qg) * (1.0f + qu)) * (1.0f + r);
+  const float mag = bb * __fdividef(num, den);
+  return ((g < 0.0f) != (u < 0.0f)) ? -mag : mag;
+}
+
+// One 32-column chunk (token columns c0..c0+31) of the 128 x BN accumulator
+// of weight tile mt, read from TMEM at `tacc` (the accumulator's first column,
+// lane quarter included).  Called by the four warps of one epilogue group
+// (warp eq of the group reads lane quarter q).
+//   FC2: fp32 stores of rows 128*mt + lane to y of each column's routed slot.
+//   FC1: the group stages the chunk in smem (`stg`, 128 x 33 floats), then
+//        each thread takes 16 consecutive intermediate columns of one token:
+//        SiTU of (gate, up) = (tile rows i, 64 + i), the MXFP8 scale of the
+//        32-group (amax over two threads), E4M3 codes as one 16-byte store.
+template <bool FC1, int NCH>
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk, int mt, uint32_t tacc, int c0,
+                                               float* stg, int q, int eq, int lane, int grp) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(tacc + c0, r);
+  tmem_ld_wait();
+  if (!FC1) {
+    const int h = 128 * mt + 32 * q + lane;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int col = c0 + jj;
+      if (col < wk.n) {
+        const int slot = __ldg(a.slot_of_row + wk.r0 + col);
+        a.y[static_cast<size_t>(slot) * a.H + h] = __uint_as_float(r[jj]);
+      }
+    }
+    return;
+  }
+  float* row = stg + (32 * q + lane) * 33;
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) row[jj] = __uint_as_float(r[jj]);
+  named_barrier(2 + grp, 128);
+  {
+    // thread -> (column, 32-group of the 64 intermediate indices, half)
+    const int t = eq * 32 + lane;
+    const int cl = t >> 2;
+    const int gh = (t >> 1) & 1;
+    const int hh = t & 1;
+    const int col = c0 + cl;
+    const int i0 = 32 * gh + 16 * hh;
+    float act[16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float g = stg[(i0 + i) * 33 + cl];
+      const float u = stg[(64 + i0 + i) * 33 + cl];
+      act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
+      amax = fmaxf(amax, fabsf(act[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the other half of the group
+    const int e = e4m3_scale_exp(amax);
+    const float inv = exp2i(-e);
+    uint32_t w[4];
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4] * inv, act[4 * k4 + 1] * inv),
+                                                   __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4 + 2] * inv, act[4 * k4 + 3] * inv),
+                                                   __NV_SATFINITE, __NV_E4M3);
+      w[k4] = (lo & 0xFFFFu) | (hi << 16);
+    }
+    if (col < wk.n) {
+      *reinterpret_cast<uint4*>(a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+      if (hh == 0)
+        a.isf[tile_sf_offset(wk.tile, col, 2 * mt + gh, NCH, a.I / 128)] = static_cast<uint8_t>(e + 127);
+    }
+  }
+  named_barrier(2 + grp, 128);
+}
+
+}  // namespace kmoe

@@ -1,0 +1,311 @@
+// CTA-pair variant of the grouped expert GEMMs for the 224-row token tiles
+// of prefill-sized layers.
+//
+// A cluster of two CTAs (two SMs) runs one work item = (expert e, weight
+// tiles 2m and 2m+1, token tile of up to 224 rows) as 56 (FC1) or 28 (FC2)
+// K blocks of tcgen05.mma.cta_group::2 with M = 256: CTA r supplies weight
+// tile 2m+r (its 128 A rows) and half of the token rows, and its TMEM receives
+// the 128 x 224 accumulator of its own weight tile.  Compared with one CTA
+// computing both weight tiles, every SM loads half the token rows per K block
+// and its shared memory serves the token operand once for both tensor cores,
+// and each TMEM holds one 224-column accumulator, so two fit: the epilogue of
+// one item overlaps the main loop of the next.
+//
+// Roles in each CTA of the pair:
+//   warp 0      TMA of the CTA's weight block and its 512 scale bytes
+//   warp 1      even CTA: TMEM owner and issuer of the pair MMAs (one lane);
+//               odd CTA: relays "stage s of this CTA is loaded" to the even
+//               CTA's full barrier (a cluster-scope arrive)
+//   warps 2..9  epilogue on the CTA's own accumulator (as in the one-CTA kernel)
+//   warp 10     TMA of the CTA's token rows (token tile rows [rN/2, rN/2+112))
+//               and of the scales of all token rows of the tile
+// Barriers: full[s] of the even CTA completes when its own two producers and
+// the odd CTA's relay have arrived; the MMA commit multicasts empty[s] and
+// acc_full[b] to both CTAs; acc_empty[b] of the even CTA counts the epilogue
+// warps of both CTAs.  Every wait is bounded.
+#include "gemm_dev.cuh"
+
+namespace kmoe {
+
+template <bool FC1_, int STAGES_>
+struct PairCfg {
+  static constexpr bool FC1 = FC1_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int BN = 224;         // token rows per item (both CTAs)
+  static constexpr int HALF = BN / 2;    // token rows loaded by each CTA
+  static constexpr int NCH = 2;          // 128-row scale chunks of a token tile
+  static constexpr int NT = 2;           // weight tiles per item (one per CTA)
+  static constexpr int A_KB = 16384;     // 128 rows x 128 FP4 in the unpacked smem format
+  static constexpr int A_TX = 8192;      // transaction bytes of that tile (packed source)
+  static constexpr int B_OFF = A_KB;
+  static constexpr int B_BYTES = HALF * 128;
+  static constexpr int SFA_OFF = B_OFF + B_BYTES;
+  static constexpr int SFB_OFF = SFA_OFF + 512;
+  static constexpr int STAGE = (SFB_OFF + NCH * 512 + 1023) / 1024 * 1024;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int NGRP = EPI_WARPS / 4;
+  static constexpr int PRODB_WARP = 2 + EPI_WARPS;
+  static constexpr int THREADS = 32 * (3 + EPI_WARPS);
+  static constexpr int STG_FLOATS = 128 * 33;
+  static constexpr int STG_BYTES = FC1 ? NGRP * STG_FLOATS * 4 : 0;
+  static constexpr int BAR_OFF = STAGES * STAGE + STG_BYTES;
+  static constexpr int TS_OFF = BAR_OFF + 256;  // shared copy of tile_start
+  static constexpr int SMEM = 1024 + TS_OFF + kTileStartBytes;
+  static constexpr int NACC = 2;
+  static constexpr int SF_COL0 = NACC * BN;  // scale columns after the two accumulators
+  static constexpr int SFW = 4 + 4 * NCH;    // per stage: own A scales, then all token-row scales
+  static constexpr int TMEM_COLS = 512;
+  static_assert(SF_COL0 + STAGES * SFW <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(B_OFF % 1024 == 0 && STAGE % 1024 == 0, "128-byte-swizzled operands start on 1 KB");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __grid_constant__ GemmMaps maps,
+                                                                     const GemmArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* tsm = reinterpret_cast<int32_t*>(smem + C::TS_OFF);
+  stage_tile_start(a, tsm);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool lead = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], lead ? 3 : 2);  // two producers (+ the odd CTA's relay)
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < C::NACC; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * C::EPI_WARPS);  // epilogue warps of both CTAs
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.b[4]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int total = (a.MT / C::NT) * tsm[a.E];
+  const uint64_t budget = a.budget_ns;
+
+  if (warp == 0 || warp == C::PRODB_WARP) {
+    // ------------------------------------------------------------ producers
+    if (lane == 0) {
+      const bool is_a = warp == 0;
+      const uint64_t pol = is_a ? policy_evict_normal() : policy_evict_last();
+      const uint32_t tx = is_a ? C::A_TX + 512 : C::B_BYTES + C::NCH * 512;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int w = pair; w < total && ok; w += npairs) {
+        Work wk;
+        decode_work(a, tsm, C::BN, C::NT, w, wk);
+        const int half = static_cast<int>(((static_cast<uint32_t>(wk.n) + 15u) & ~15u) >> 1);
+        const int blk0 = (wk.e * a.MT + C::NT * wk.m + static_cast<int>(rank)) * a.KB;
+        const uint8_t* bsf = a.bsf + static_cast<size_t>(wk.tile) * a.KB * C::NCH * 512;
+        for (int kb = 0; kb < a.KB; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * C::STAGE;
+          mbar_arrive_expect_tx(&full[s], tx);
+          if (is_a) {
+            tma_load_3d(st, &maps.a, &full[s], 0, 0, blk0 + kb, pol);
+            bulk_load(st + C::SFA_OFF, a.wsf + static_cast<size_t>(blk0 + kb) * 512, 512, &full[s]);
+          } else {
+            // this CTA's half of the MMA's token rows (rows past the tile are
+            // loaded but not used; rows past the tensor read as zero)
+            tma_load_2d(st + C::B_OFF, &maps.b[4], &full[s], kb * 128, wk.r0 + static_cast<int>(rank) * half, pol);
+            bulk_load(st + C::SFB_OFF, bsf + static_cast<size_t>(kb) * C::NCH * 512, C::NCH * 512, &full[s]);
+          }
+        }
+      }
+      if (!ok) {
+        const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
+        for (uint32_t i = first; i < it; ++i)
+          mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1u, 20000000ull, nullptr, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && !lead) {
+      // ---------------------------------------------------------- relay (odd CTA)
+      const uint32_t lead_full = cluster_map(full, 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int w = pair; w < total && ok; w += npairs) {
+        for (int kb = 0; kb < a.KB; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          if (!mbar_wait_bounded(&full[s], (it / C::STAGES) & 1u, budget, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(lead_full + 8u * s);
+        }
+      }
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      // The tensor pipe takes the next MMA only about as fast as it runs one,
+      // so this loop stays lean: descriptors are formed once and advanced by
+      // adds (the start-address field holds smem offset >> 4), stage and
+      // phase advance incrementally.
+      constexpr uint32_t kStageD = C::STAGE >> 4;
+      const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
+      const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + C::B_OFF));
+      const uint64_t sfadesc0 = sdesc_sf_32x16(smem_u32(smem + C::SFA_OFF));
+      const uint64_t sfbdesc0 = sdesc_sf_32x16(smem_u32(smem + C::SFB_OFF));
+      const uint32_t sf_base = tmem + C::SF_COL0;
+      int s = 0;
+      uint32_t ph = 0, li = 0;
+      bool ok = true;
+      for (int w = pair; w < total && ok; w += npairs, ++li) {
+        Work wk;
+        decode_work(a, tsm, C::BN, C::NT, w, wk);
+        const uint32_t acc = li & 1u;
+        if (!mbar_wait_bounded<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * C::BN;
+        const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
+        const bool two_chunks = nmma > 128u;
+        const uint32_t id0 = idesc_mxf8f6f4(256, nmma, MX_E2M1, MX_E4M3, 0, 0);
+        const uint32_t id1 = id0 | (1u << 4) | (1u << 29);
+        const uint32_t id2 = id0 | (2u << 4) | (2u << 29);
+        const uint32_t id3 = id0 | (3u << 4) | (3u << 29);
+        for (int kb = 0; kb < a.KB; ++kb) {
+          if (!mbar_wait_bounded<true>(&full[s], ph, budget, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = static_cast<uint64_t>(s) * kStageD;
+          const uint32_t sfa = sf_base + static_cast<uint32_t>(s) * C::SFW;
+          tc_cp_32x128b_warpx4_pair(sfa, sfadesc0 + so);
+          tc_cp_32x128b_warpx4_pair(sfa + 4, sfbdesc0 + so);
+          if (two_chunks) tc_cp_32x128b_warpx4_pair(sfa + 8, sfbdesc0 + so + 32);
+          const uint64_t ad = adesc0 + so, bd = bdesc0 + so;
+          mma_mxf8f6f4_pair(d, ad, bd, id0, sfa, sfa + 4, kb != 0);
+          mma_mxf8f6f4_pair(d, ad + 2, bd + 2, id1, sfa, sfa + 4, 1u);
+          mma_mxf8f6f4_pair(d, ad + 4, bd + 4, id2, sfa, sfa + 4, 1u);
+          mma_mxf8f6f4_pair(d, ad + 6, bd + 6, id3, sfa, sfa + 4, 1u);
+          tc_commit_pair(&empty[s]);
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(&acc_full[acc]);
+      }
+      tc_commit_pair(done);
+      mbar_wait_bounded(done, 0, budget, a.err, nullptr);
+    }
+  } else if (warp < C::PRODB_WARP) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const int grp = ew >> 2;
+    const int eq = ew & 3;
+    float* stg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE) + grp * C::STG_FLOATS;
+    const uint32_t lead_acc_empty = cluster_map(acc_empty, 0);
+    uint32_t li = 0;
+    for (int w = pair; w < total; w += npairs, ++li) {
+      Work wk;
+      decode_work(a, tsm, C::BN, C::NT, w, wk);
+      const uint32_t acc = li & 1u;
+      const uint32_t aph = (li >> 1) & 1u;
+      bool ok = mbar_wait_bounded(&acc_full[acc], aph, budget, a.err, abort_flag);
+      ok = named_barrier_and(1, 32 * C::EPI_WARPS, ok && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int mt = C::NT * wk.m + static_cast<int>(rank);  // this CTA's weight tile
+      const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::BN;
+      const int nchunk = (wk.n + 31) >> 5;
+      for (int ci = grp; ci < nchunk; ci += C::NGRP)
+        epilogue_chunk<C::FC1, C::NCH>(a, wk, mt, tacc, ci * 32, stg, q, eq, lane, grp);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (lead)
+          mbar_arrive(&acc_empty[acc]);
+        else
+          mbar_arrive_remote(lead_acc_empty + 8u * acc);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no MMA of the pair and no remote arrive is outstanding past here
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+}
+
+template <class C>
+static cudaError_t launch_pair(const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
+  static int pairs = 0;  // co-resident clusters of two (per instantiation; idempotent)
+  if (pairs == 0) {
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_pair_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, moe_gemm_pair_kernel<C>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    pairs = n < sms / 2 ? n : sms / 2;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<C>, maps, a);
+}
+
+cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
+  if (a.MT % 2 != 0) return cudaErrorInvalidValue;
+  return fc1 ? launch_pair<PairCfg<true, 5>>(maps, a, sms, st) : launch_pair<PairCfg<false, 5>>(maps, a, sms, st);
+}
+
+}  // namespace kmoe

@@ -55,19 +55,19 @@ __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ log
   }
   // pass 1: the k-th largest cheap key, by a bitwise radix select over
   // order-preserving integer images of the keys (32 counting rounds)
-  uint32_t okey[KPL];
+  uint32_t okey[KPL];  // 0 for absent experts: below every probe
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const uint32_t u = __float_as_uint(key[i]);
-    okey[i] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    okey[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
   }
   uint32_t prefix = 0;
   for (int bit = 31; bit >= 0; --bit) {
     const uint32_t probe = prefix | (1u << bit);
-    int cnt = 0;
+    unsigned cnt = 0;
 #pragma unroll
-    for (int i = 0; i < KPL; ++i) cnt += (lane + 32 * i < E && okey[i] >= probe) ? 1 : 0;
-    if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt))) >= k) prefix = probe;
+    for (int i = 0; i < KPL; ++i) cnt += okey[i] >= probe;
+    if (static_cast<int>(__reduce_add_sync(0xffffffffu, cnt)) >= k) prefix = probe;
   }
   const float kth = __uint_as_float((prefix & 0x80000000u) ? (prefix & 0x7fffffffu) : ~prefix);
 

@@ -17,6 +17,11 @@ from tests._moe_setup import (assert_output_parity, device_inputs, device_weight
 pytestmark = pytest.mark.gpu
 
 TINY_UNSAT = W.WORKLOADS["tiny"].with_(name="tiny_unsaturated", sf_lo=117, sf_hi=121)
+# 224-row token tiles (the CTA-pair GEMMs) at sizes the oracle checks on every
+# token: 256 rows per expert on average, several work items per CTA pair,
+# full and partial tiles; the skewed bias gives experts of 1 to ~1000 rows.
+PAIR_EVEN = W.WORKLOADS["tiny"].with_(name="pair_tiles", T=4096, H=512, I=512, E=32, k=2)
+PAIR_SKEW = PAIR_EVEN.with_(name="pair_tiles_skewed", skewed=True)
 
 
 @pytest.fixture(scope="module")
@@ -67,6 +72,18 @@ def test_forward_tiny_full(K, wl):
     tokens = np.arange(wl.T)
     ref = oracle_forward(wl, s, tokens)
     _check_stages(wl, p, ws, s, ref, tokens)
+    assert_output_parity(out, ref["out"], wl.name)
+
+
+@pytest.mark.parametrize("wl", [PAIR_EVEN, PAIR_SKEW], ids=["even", "skewed"])
+def test_forward_pair_tiles_every_token(K, wl):
+    out, ws, p, s, _ = run_forward(wl)
+    assert K.kmoe_workspace_layout(p).tile_rows == 224
+    tokens = np.arange(wl.T)
+    ref = oracle_forward(wl, s, tokens)
+    st = _check_stages(wl, p, ws, s, ref, tokens)
+    counts = st["counts"]
+    assert counts.max() > 224 and (counts % 224 != 0).any()  # multi-tile experts and partial tiles
     assert_output_parity(out, ref["out"], wl.name)
 
 
