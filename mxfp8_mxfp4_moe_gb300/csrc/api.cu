@@ -50,7 +50,7 @@ EncodeTiledFn encode_fn() {
 
 // 2-D tensor map over [rows, cols] elements with row stride `stride_bytes`.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
-              uint64_t stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+              uint64_t stride_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128 = true) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[2] = {cols, rows};
@@ -58,7 +58,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(base), gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -264,6 +264,16 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   GemmMaps m1, m2;
   if (!make_weight_map(&m1.a, w13_k, weight_blocks(p, 0), kps1) ||
       !make_weight_map(&m2.a, w2_k, weight_blocks(p, 1), kps2))
+    return KMOE_ERR_CUDA;
+  // the scale regions as rows of 128 bytes (the CTA-pair kernel loads them by TMA)
+  const uint64_t sf1_rows = static_cast<uint64_t>(H / 128) * L.max_tiles * L.nch * 4;
+  const uint64_t sf2_rows = static_cast<uint64_t>(I / 128) * L.max_tiles * L.nch * 4;
+  if (!make_map(&m1.asf, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13_k + weight_blocks(p, 0) * 8192, 128,
+                weight_blocks(p, 0) * 4, 128, 128, 4, false) ||
+      !make_map(&m2.asf, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2_k + weight_blocks(p, 1) * 8192, 128,
+                weight_blocks(p, 1) * 4, 128, 128, 4, false) ||
+      !make_map(&m1.bsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, xsf, 128, sf1_rows, 128, 128, 4 * L.nch, false) ||
+      !make_map(&m2.bsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, isf, 128, sf2_rows, 128, 128, 4 * L.nch, false))
     return KMOE_ERR_CUDA;
   for (int i = 0; i < 5; ++i) {
     // 32, 64, 128 rows, one tile, half a tile

@@ -64,7 +64,7 @@ struct GemmCfg {
   static constexpr int NGRP = EPI_WARPS / 4;      // epilogue groups (column-chunk interleave)
   static constexpr int PRODB_WARP = 2 + EPI_WARPS;  // second producer: token rows and their scales
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
-  static constexpr int STG_FLOATS = 128 * 33;  // one 128 x 32 staging tile (padded rows) per group
+  static constexpr int STG_FLOATS = kStgFloats;  // one 128 x 32 staging tile per group
   static constexpr int STG_BYTES = FC1 ? NGRP * STG_FLOATS * 4 : 0;
   static constexpr int BAR_OFF = STAGES * STAGE + STG_BYTES;
   static constexpr int TS_OFF = BAR_OFF + 256;  // shared copy of tile_start
@@ -371,7 +371,7 @@ cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, con
     if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 3, true>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<64, 1, 6, true>>(maps, a, grid, st);
     if (BN == 224 && kps == 1)
-      return a.MT % 2 == 0 ? launch_one<GemmCfg<224, 1, 3, true, 8, 1, 2>>(maps, a, grid, st)
+      return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(true, maps, a, grid, st)
                            : launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
   } else {
     if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2>>(maps, a, grid, st)
@@ -379,7 +379,7 @@ cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, con
     if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 4, false>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<64, 1, 7, false>>(maps, a, grid, st);
     if (BN == 224 && kps == 1)
-      return a.MT % 2 == 0 ? launch_one<GemmCfg<224, 1, 3, false, 8, 1, 2>>(maps, a, grid, st)
+      return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(false, maps, a, grid, st)
                            : launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st);
   }
   return cudaErrorInvalidValue;

@@ -14,6 +14,8 @@ constexpr int kWeightBlockBytes = 8192 + 512;
 struct GemmMaps {
   CUtensorMap a;
   CUtensorMap b[5];
+  CUtensorMap asf;  // weight scales as rows of 128 B, box of 4 rows (one block)
+  CUtensorMap bsf;  // token-tile scales as rows of 128 B, box of one K block of a tile
 };
 
 // K blocks (of 128) moved per pipeline stage for a token-tile size and a K
@@ -50,8 +52,10 @@ cudaError_t launch_prep_weights(const uint8_t* codes, const uint8_t* sf, uint8_t
 cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, const GemmArgs& a, int grid,
                             cudaStream_t st);
 
-// The CTA-pair kernel for BN = 224 (gemm_pair.cu); a.MT must be even.  `sms`
-// is the SM count; the grid is the number of co-resident pairs.
+// The CTA-pair kernel for BN = 224 (gemm_pair.cu): weight tiles per expert
+// (MT) and K blocks (KB) must both be even.  `sms` is the SM count; the grid
+// is the number of co-resident pairs.
+bool pair_gemm_supported(int MT, int KB);
 cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st);
 
 }  // namespace kmoe

@@ -85,12 +85,20 @@ __device__ __forceinline__ float situ_f32(float g, float u, float kg, float ku, 
   return ((g < 0.0f) != (u < 0.0f)) ? -mag : mag;
 }
 
+// Epilogue staging tile: 128 rows x 32 floats, unpadded.  The 16-byte unit u
+// of row r is stored at unit u ^ (r & 7) ^ ((r >> 4) & 3), which keeps both
+// the row-wise float4 writes and the column reads of the SiTU step at most
+// two-way bank-conflicted.
+constexpr int kStgFloats = 128 * 32;
+__device__ __forceinline__ int stg_unit(int r, int u) { return r * 32 + ((u ^ (r & 7) ^ ((r >> 4) & 3)) << 2); }
+__device__ __forceinline__ int stg_at(int r, int c) { return stg_unit(r, c >> 2) + (c & 3); }
+
 // One 32-column chunk (token columns c0..c0+31) of the 128 x BN accumulator
 // of weight tile mt, read from TMEM at `tacc` (the accumulator's first column,
 // lane quarter included).  Called by the four warps of one epilogue group
 // (warp eq of the group reads lane quarter q).
 //   FC2: fp32 stores of rows 128*mt + lane to y of each column's routed slot.
-//   FC1: the group stages the chunk in smem (`stg`, 128 x 33 floats), then
+//   FC1: the group stages the chunk in smem (`stg`, 128 x 32 floats), then
 //        each thread takes 16 consecutive intermediate columns of one token:
 //        SiTU of (gate, up) = (tile rows i, 64 + i), the MXFP8 scale of the
 //        32-group (amax over two threads), E4M3 codes as one 16-byte store.
@@ -112,9 +120,14 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
     }
     return;
   }
-  float* row = stg + (32 * q + lane) * 33;
+  {
+    const int rr = 32 * q + lane;
 #pragma unroll
-  for (int jj = 0; jj < 32; ++jj) row[jj] = __uint_as_float(r[jj]);
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<float4*>(stg + stg_unit(rr, u)) =
+          make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]), __uint_as_float(r[4 * u + 2]),
+                      __uint_as_float(r[4 * u + 3]));
+  }
   named_barrier(2 + grp, 128);
   {
     // thread -> (column, 32-group of the 64 intermediate indices, half)
@@ -128,8 +141,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float g = stg[(i0 + i) * 33 + cl];
-      const float u = stg[(64 + i0 + i) * 33 + cl];
+      const float g = stg[stg_at(i0 + i, cl)];
+      const float u = stg[stg_at(64 + i0 + i, cl)];
       act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
       amax = fmaxf(amax, fabsf(act[i]));
     }

@@ -13,16 +13,15 @@
 //
 // Roles in each CTA of the pair:
 //   warp 0      TMA of the CTA's weight block and its 512 scale bytes
-//   warp 1      even CTA: TMEM owner and issuer of the pair MMAs (one lane);
-//               odd CTA: relays "stage s of this CTA is loaded" to the even
-//               CTA's full barrier (a cluster-scope arrive)
+//   warp 1      TMEM allocation (both CTAs); in the even CTA one lane issues
+//               the pair MMAs
 //   warps 2..9  epilogue on the CTA's own accumulator (as in the one-CTA kernel)
 //   warp 10     TMA of the CTA's token rows (token tile rows [rN/2, rN/2+112))
 //               and of the scales of all token rows of the tile
-// Barriers: full[s] of the even CTA completes when its own two producers and
-// the odd CTA's relay have arrived; the MMA commit multicasts empty[s] and
-// acc_full[b] to both CTAs; acc_empty[b] of the even CTA counts the epilogue
-// warps of both CTAs.  Every wait is bounded.
+// Barriers: every load of both CTAs completes on full[s] of the even CTA (TMA
+// .cta_group::2), whose two producers expect the bytes of both CTAs; the MMA
+// commit multicasts empty[s] and acc_full[b] to both CTAs; acc_empty[b] of the
+// even CTA counts the epilogue warps of both CTAs.  Every wait is bounded.
 #include "gemm_dev.cuh"
 
 namespace kmoe {
@@ -31,33 +30,40 @@ template <bool FC1_, int STAGES_>
 struct PairCfg {
   static constexpr bool FC1 = FC1_;
   static constexpr int STAGES = STAGES_;
+  static constexpr int KPS = 2;          // 128-wide K blocks per stage (8 pair MMAs)
   static constexpr int BN = 224;         // token rows per item (both CTAs)
   static constexpr int HALF = BN / 2;    // token rows loaded by each CTA
   static constexpr int NCH = 2;          // 128-row scale chunks of a token tile
   static constexpr int NT = 2;           // weight tiles per item (one per CTA)
   static constexpr int A_KB = 16384;     // 128 rows x 128 FP4 in the unpacked smem format
   static constexpr int A_TX = 8192;      // transaction bytes of that tile (packed source)
-  static constexpr int B_OFF = A_KB;
   static constexpr int B_BYTES = HALF * 128;
-  static constexpr int SFA_OFF = B_OFF + B_BYTES;
-  static constexpr int SFB_OFF = SFA_OFF + 512;
-  static constexpr int STAGE = (SFB_OFF + NCH * 512 + 1023) / 1024 * 1024;
-  static constexpr int EPI_WARPS = 8;
+  // stage: A[kbi] (16 KB each), B[kbi] (112 rows), SFA[kbi] (512 B), SFB[kbi] (1 KB)
+  static constexpr int B_OFF = KPS * A_KB;
+  static constexpr int SFA_OFF = B_OFF + KPS * B_BYTES;
+  static constexpr int SFB_OFF = SFA_OFF + KPS * 512;
+  static constexpr int STAGE = (SFB_OFF + KPS * NCH * 512 + 1023) / 1024 * 1024;
+  static constexpr int EPI_WARPS = 4;  // one per TMEM lane quarter (fewer share the MMA warp's scheduler)
   static constexpr int NGRP = EPI_WARPS / 4;
   static constexpr int PRODB_WARP = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
-  static constexpr int STG_FLOATS = 128 * 33;
+  static constexpr int STG_FLOATS = kStgFloats;
   static constexpr int STG_BYTES = FC1 ? NGRP * STG_FLOATS * 4 : 0;
   static constexpr int BAR_OFF = STAGES * STAGE + STG_BYTES;
   static constexpr int TS_OFF = BAR_OFF + 256;  // shared copy of tile_start
   static constexpr int SMEM = 1024 + TS_OFF + kTileStartBytes;
   static constexpr int NACC = 2;
   static constexpr int SF_COL0 = NACC * BN;  // scale columns after the two accumulators
-  static constexpr int SFW = 4 + 4 * NCH;    // per stage: own A scales, then all token-row scales
+  static constexpr int SFW = 4 + 4 * NCH;    // per K block: own A scales, then all token-row scales
+  static constexpr int SF_SLOT = KPS * SFW;  // per stage
   static constexpr int TMEM_COLS = 512;
-  static_assert(SF_COL0 + STAGES * SFW <= TMEM_COLS, "TMEM budget");
+  // Two scale slots alternate by stage: the copies into a slot are issued
+  // after the MMAs that read its previous contents (the tcgen05 operations
+  // of one thread run in issue order).
+  static_assert(SF_COL0 + 2 * SF_SLOT <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(B_OFF % 1024 == 0 && STAGE % 1024 == 0, "128-byte-swizzled operands start on 1 KB");
+  static_assert(B_OFF % 1024 == 0 && B_BYTES % 1024 == 0 && STAGE % 1024 == 0,
+                "128-byte-swizzled operands start on 1 KB");
 };
 
 template <class C>
@@ -72,6 +78,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
   uint64_t* done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // MMA width of item li in item_n[li & 3], written by the token producer
+  // before it arrives on the item's first stage (so the MMA thread decodes nothing)
+  volatile uint32_t* item_n = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
   int32_t* tsm = reinterpret_cast<int32_t*>(smem + C::TS_OFF);
   stage_tile_start(a, tsm);
 
@@ -81,7 +90,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
   const bool lead = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], lead ? 3 : 2);  // two producers (+ the odd CTA's relay)
+      mbar_init(&full[s], 2);  // the even CTA's two producers (plus both CTAs' bytes)
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < C::NACC; ++b) {
@@ -99,6 +108,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.a);
     prefetch_tmap(&maps.b[4]);
+    prefetch_tmap(&maps.asf);
+    prefetch_tmap(&maps.bsf);
   }
   tc_fence_before();
   __syncthreads();
@@ -112,19 +123,24 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
 
   if (warp == 0 || warp == C::PRODB_WARP) {
     // ------------------------------------------------------------ producers
+    // Both CTAs' loads complete on the even CTA's full barrier (the TMA
+    // .cta_group::2 form); its producers expect the bytes of both CTAs.
     if (lane == 0) {
       const bool is_a = warp == 0;
       const uint64_t pol = is_a ? policy_evict_normal() : policy_evict_last();
-      const uint32_t tx = is_a ? C::A_TX + 512 : C::B_BYTES + C::NCH * 512;
-      uint32_t it = 0;
+      const uint32_t tx2 = 2u * C::KPS * (is_a ? C::A_TX + 512 : C::B_BYTES + C::NCH * 512);
+      const uint32_t lead_full = cluster_map(full, 0);
+      uint32_t it = 0, li = 0;
       bool ok = true;
-      for (int w = pair; w < total && ok; w += npairs) {
+      for (int w = pair; w < total && ok; w += npairs, ++li) {
         Work wk;
         decode_work(a, tsm, C::BN, C::NT, w, wk);
-        const int half = static_cast<int>(((static_cast<uint32_t>(wk.n) + 15u) & ~15u) >> 1);
+        const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
+        const int half = static_cast<int>(nmma >> 1);
         const int blk0 = (wk.e * a.MT + C::NT * wk.m + static_cast<int>(rank)) * a.KB;
-        const uint8_t* bsf = a.bsf + static_cast<size_t>(wk.tile) * a.KB * C::NCH * 512;
-        for (int kb = 0; kb < a.KB; ++kb, ++it) {
+        const int sfrow0 = wk.tile * a.KB * C::NCH * 4;  // token-tile scale rows of K block 0
+        const int brow = wk.r0 + static_cast<int>(rank) * half;
+        for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
@@ -132,85 +148,88 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
             break;
           }
           uint8_t* st = smem + s * C::STAGE;
-          mbar_arrive_expect_tx(&full[s], tx);
-          if (is_a) {
-            tma_load_3d(st, &maps.a, &full[s], 0, 0, blk0 + kb, pol);
-            bulk_load(st + C::SFA_OFF, a.wsf + static_cast<size_t>(blk0 + kb) * 512, 512, &full[s]);
-          } else {
-            // this CTA's half of the MMA's token rows (rows past the tile are
-            // loaded but not used; rows past the tensor read as zero)
-            tma_load_2d(st + C::B_OFF, &maps.b[4], &full[s], kb * 128, wk.r0 + static_cast<int>(rank) * half, pol);
-            bulk_load(st + C::SFB_OFF, bsf + static_cast<size_t>(kb) * C::NCH * 512, C::NCH * 512, &full[s]);
+          const uint32_t bar = lead_full + 8u * s;
+          if (lead) {
+            if (!is_a && kb == 0) item_n[li & 3u] = nmma;
+            mbar_arrive_expect_tx(&full[s], tx2);
+          }
+#pragma unroll
+          for (int kbi = 0; kbi < C::KPS; ++kbi) {
+            if (is_a) {
+              tma_load_3d_pair(st + kbi * C::A_KB, &maps.a, bar, 0, 0, blk0 + kb + kbi, pol);
+              tma_load_2d_pair(st + C::SFA_OFF + kbi * 512, &maps.asf, bar, 0, 4 * (blk0 + kb + kbi), pol);
+            } else {
+              // this CTA's half of the MMA's token rows (rows past the tile are
+              // loaded but not used; rows past the tensor read as zero)
+              tma_load_2d_pair(st + C::B_OFF + kbi * C::B_BYTES, &maps.b[4], bar, (kb + kbi) * 128, brow, pol);
+              tma_load_2d_pair(st + C::SFB_OFF + kbi * C::NCH * 512, &maps.bsf, bar, 0,
+                               sfrow0 + (kb + kbi) * C::NCH * 4, pol);
+            }
           }
         }
       }
       if (!ok) {
-        const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
-        for (uint32_t i = first; i < it; ++i)
-          mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1u, 20000000ull, nullptr, nullptr);
+        // let the copies already issued land before the CTA can exit
+        if (lead) {
+          const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
+          for (uint32_t i = first; i < it; ++i)
+            mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1u, 20000000ull, nullptr, nullptr);
+        } else {
+          spin_ns(100000ull);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && !lead) {
-      // ---------------------------------------------------------- relay (odd CTA)
-      const uint32_t lead_full = cluster_map(full, 0);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int w = pair; w < total && ok; w += npairs) {
-        for (int kb = 0; kb < a.KB; ++kb, ++it) {
-          const int s = it % C::STAGES;
-          if (!mbar_wait_bounded(&full[s], (it / C::STAGES) & 1u, budget, a.err, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_remote(lead_full + 8u * s);
-        }
-      }
-    } else if (lane == 0) {
+    if (lane == 0 && lead) {
       // ---------------------------------------------------------- MMA issuer (even CTA)
       // The tensor pipe takes the next MMA only about as fast as it runs one,
       // so this loop stays lean: descriptors are formed once and advanced by
       // adds (the start-address field holds smem offset >> 4), stage and
-      // phase advance incrementally.
+      // phase advance incrementally, the item's MMA width comes from smem.
       constexpr uint32_t kStageD = C::STAGE >> 4;
+      constexpr uint32_t kAD = C::A_KB >> 4, kBD = C::B_BYTES >> 4;
       const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
       const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + C::B_OFF));
       const uint64_t sfadesc0 = sdesc_sf_32x16(smem_u32(smem + C::SFA_OFF));
       const uint64_t sfbdesc0 = sdesc_sf_32x16(smem_u32(smem + C::SFB_OFF));
       const uint32_t sf_base = tmem + C::SF_COL0;
       int s = 0;
-      uint32_t ph = 0, li = 0;
+      uint32_t ph = 0, li = 0, slot = 0;
       bool ok = true;
       for (int w = pair; w < total && ok; w += npairs, ++li) {
-        Work wk;
-        decode_work(a, tsm, C::BN, C::NT, w, wk);
         const uint32_t acc = li & 1u;
         if (!mbar_wait_bounded<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * C::BN;
-        const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
-        const bool two_chunks = nmma > 128u;
-        const uint32_t id0 = idesc_mxf8f6f4(256, nmma, MX_E2M1, MX_E4M3, 0, 0);
-        const uint32_t id1 = id0 | (1u << 4) | (1u << 29);
-        const uint32_t id2 = id0 | (2u << 4) | (2u << 29);
-        const uint32_t id3 = id0 | (3u << 4) | (3u << 29);
-        for (int kb = 0; kb < a.KB; ++kb) {
-          if (!mbar_wait_bounded<true>(&full[s], ph, budget, a.err, abort_flag)) {
+        uint32_t id0 = 0;
+        bool two_chunks = false;
+        for (int kb = 0; kb < a.KB; kb += C::KPS) {
+          if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          if (kb == 0) {
+            const uint32_t nmma = item_n[li & 3u];
+            two_chunks = nmma > 128u;
+            id0 = idesc_mxf8f6f4(256, nmma, MX_E2M1, MX_E4M3, 0, 0);
+          }
           const uint64_t so = static_cast<uint64_t>(s) * kStageD;
-          const uint32_t sfa = sf_base + static_cast<uint32_t>(s) * C::SFW;
-          tc_cp_32x128b_warpx4_pair(sfa, sfadesc0 + so);
-          tc_cp_32x128b_warpx4_pair(sfa + 4, sfbdesc0 + so);
-          if (two_chunks) tc_cp_32x128b_warpx4_pair(sfa + 8, sfbdesc0 + so + 32);
-          const uint64_t ad = adesc0 + so, bd = bdesc0 + so;
-          mma_mxf8f6f4_pair(d, ad, bd, id0, sfa, sfa + 4, kb != 0);
-          mma_mxf8f6f4_pair(d, ad + 2, bd + 2, id1, sfa, sfa + 4, 1u);
-          mma_mxf8f6f4_pair(d, ad + 4, bd + 4, id2, sfa, sfa + 4, 1u);
-          mma_mxf8f6f4_pair(d, ad + 6, bd + 6, id3, sfa, sfa + 4, 1u);
+          const uint32_t sf = sf_base + slot;
+#pragma unroll
+          for (int kbi = 0; kbi < C::KPS; ++kbi) {
+            const uint32_t sfa = sf + kbi * C::SFW;
+            tc_cp_32x128b_warpx4_pair(sfa, sfadesc0 + so + kbi * 32);
+            tc_cp_32x128b_warpx4_pair(sfa + 4, sfbdesc0 + so + kbi * C::NCH * 32);
+            if (two_chunks) tc_cp_32x128b_warpx4_pair(sfa + 8, sfbdesc0 + so + kbi * C::NCH * 32 + 32);
+            const uint64_t ad = adesc0 + so + kbi * kAD, bd = bdesc0 + so + kbi * kBD;
+            mma_mxf8f6f4_pair(d, ad, bd, id0, sfa, sfa + 4, (kb | kbi) != 0);
+            mma_mxf8f6f4_pair(d, ad + 2, bd + 2, id0 | (1u << 4) | (1u << 29), sfa, sfa + 4, 1u);
+            mma_mxf8f6f4_pair(d, ad + 4, bd + 4, id0 | (2u << 4) | (2u << 29), sfa, sfa + 4, 1u);
+            mma_mxf8f6f4_pair(d, ad + 6, bd + 6, id0 | (3u << 4) | (3u << 29), sfa, sfa + 4, 1u);
+          }
           tc_commit_pair(&empty[s]);
+          slot ^= C::SF_SLOT;
           if (++s == C::STAGES) {
             s = 0;
             ph ^= 1u;
@@ -303,9 +322,11 @@ static cudaError_t launch_pair(const GemmMaps& maps, const GemmArgs& a, int sms,
   return cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<C>, maps, a);
 }
 
+bool pair_gemm_supported(int MT, int KB) { return MT % 2 == 0 && KB % 2 == 0; }
+
 cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
-  if (a.MT % 2 != 0) return cudaErrorInvalidValue;
-  return fc1 ? launch_pair<PairCfg<true, 5>>(maps, a, sms, st) : launch_pair<PairCfg<false, 5>>(maps, a, sms, st);
+  if (!pair_gemm_supported(a.MT, a.KB)) return cudaErrorInvalidValue;
+  return fc1 ? launch_pair<PairCfg<true, 3>>(maps, a, sms, st) : launch_pair<PairCfg<false, 3>>(maps, a, sms, st);
 }
 
 }  // namespace kmoe
