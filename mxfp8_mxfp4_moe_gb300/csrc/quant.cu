@@ -106,8 +106,11 @@ cudaError_t launch_quant_rows(const void* x, int rows, int cols, int fmt, uint8_
 }
 
 // One block per token.  Threads 0..k-1 first resolve the token's k slots to
-// expert-sorted rows and token tiles; then each thread quantises 32-element
-// groups and writes the codes and scale byte once per routed slot.
+// expert-sorted rows and token tiles; then each thread quantises one
+// 32-element group and writes its 32 code bytes once per routed slot.  The
+// four groups of a 128-wide K block sit in an aligned quad of lanes and their
+// scale bytes are adjacent in the token-tile scale layout, so the quad merges
+// them and its first lane writes one 32-bit word per slot.
 __global__ void __launch_bounds__(256) quant_scatter_kernel(
     const __nv_bfloat16* __restrict__ x, int H, int k, int E, int BN, int nch, int max_tiles,
     const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, const int32_t* __restrict__ chunk_prefix,
@@ -135,8 +138,13 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     s_local[j] = local;
   }
   __syncthreads();
-  const int gpr = H / 32;
-  for (int g = threadIdx.x; g < gpr; g += blockDim.x) {
+  const int gpr = H / 32;  // a multiple of 4: quads are wholly in or out of range
+  const int KB = H / 128;
+  for (int g0 = 0; g0 < gpr; g0 += blockDim.x) {
+    const int g = g0 + static_cast<int>(threadIdx.x);
+    const bool active = g < gpr;
+    const unsigned mask = __ballot_sync(0xffffffffu, active);
+    if (!active) continue;
     float v[32];
     load_group_bf16(x + static_cast<size_t>(t) * H + 32 * g, v);
     const int e = e4m3_scale_exp(group_amax(v));
@@ -144,13 +152,17 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     e4m3_group(v, exp2i(-e), out);
     const uint4 lo = make_uint4(out[0], out[1], out[2], out[3]);
     const uint4 hi = make_uint4(out[4], out[5], out[6], out[7]);
+    uint32_t sc = static_cast<uint32_t>(e + 127) << (8 * (g & 3));
+    sc |= __shfl_xor_sync(mask, sc, 1);
+    sc |= __shfl_xor_sync(mask, sc, 2);
     for (int j = 0; j < k; ++j) {
       const int row = s_row[j];
       if (row < 0) continue;
       uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(row) * H + 32 * g);
       dst[0] = lo;
       dst[1] = hi;
-      xsf[tile_sf_offset(s_tile[j], s_local[j], g, nch, H / 128)] = static_cast<uint8_t>(e + 127);
+      if ((g & 3) == 0)
+        *reinterpret_cast<uint32_t*>(xsf + tile_sf_offset(s_tile[j], s_local[j], g, nch, KB)) = sc;
     }
   }
 }

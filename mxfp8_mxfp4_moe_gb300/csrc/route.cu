@@ -33,6 +33,26 @@ __device__ __forceinline__ void warp_argmax(float& key, int& idx) {
   }
 }
 
+// Order-preserving image of a non-NaN float as an unsigned integer (-0 and
+// +0 map to the same value).
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_inverse(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+// Exact selection key of expert e (NaN -> -inf) and its sigmoid score.
+__device__ __forceinline__ float exact_key(const float* lg, const float* bias, int e, float& score) {
+  score = sigmoid_exact_f32(lg[e]);
+  const float kx = score + bias[e];
+  return isnan(kx) ? -__int_as_float(0x7f800000) : kx;
+}
+
+// Only the integer images of the cheap keys live in registers (KPL per
+// lane); the candidates' exact keys are computed from the shared-memory copy
+// of the token's logits and the bias.
 template <int KPL>
 __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                                     int T, int E, int k, int32_t* __restrict__ ids,
@@ -43,24 +63,30 @@ __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ log
   const float* lg = logits + static_cast<size_t>(warp) * E;
   const float NEG_INF = -__int_as_float(0x7f800000);
 
-  float lgt[KPL], b[KPL], key[KPL];
+  // the token's logits and the bias through shared memory: all loads are
+  // independent and in flight together before any key is computed
+  __shared__ float s_lg[KPL * 32], s_b[KPL * 32];
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = lane + 32 * i;
-    lgt[i] = e < E ? lg[e] : 0.f;
-    b[i] = e < E ? bias[e] : 0.f;
-    float s = 1.f / (1.f + expf(-lgt[i]));
-    float kf = s + b[i];
-    key[i] = (e < E && !isnan(kf)) ? kf : NEG_INF;
+    if (e < E) {
+      s_lg[e] = __ldg(lg + e);
+      s_b[e] = __ldg(bias + e);
+    }
   }
-  // pass 1: the k-th largest cheap key, by a bitwise radix select over
-  // order-preserving integer images of the keys (32 counting rounds)
+  __syncwarp();
   uint32_t okey[KPL];  // 0 for absent experts: below every probe
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
-    const uint32_t u = __float_as_uint(key[i]);
-    okey[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+    const int e = lane + 32 * i;
+    okey[i] = 0u;
+    if (e < E) {
+      const float kf = 1.f / (1.f + expf(-s_lg[e])) + s_b[e];
+      okey[i] = order_key(isnan(kf) ? NEG_INF : kf);
+    }
   }
+  // pass 1: the k-th largest cheap key, by a bitwise radix select over the
+  // integer images (32 counting rounds)
   uint32_t prefix = 0;
   for (int bit = 31; bit >= 0; --bit) {
     const uint32_t probe = prefix | (1u << bit);
@@ -69,36 +95,30 @@ __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ log
     for (int i = 0; i < KPL; ++i) cnt += okey[i] >= probe;
     if (static_cast<int>(__reduce_add_sync(0xffffffffu, cnt)) >= k) prefix = probe;
   }
-  const float kth = __uint_as_float((prefix & 0x80000000u) ? (prefix & 0x7fffffffu) : ~prefix);
+  const float kth = order_key_inverse(prefix);
+  // candidates: cheap key within the margin of the k-th
+  const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
+  const uint32_t ocut = order_key((kth == NEG_INF) ? NEG_INF : kth - margin);
 
-  // fast path: gather the candidates (cheap key within the margin of the k-th)
-  // into one lane each, take their exact keys and rank them across the warp
+  // fast path: the candidates one per lane, exact keys ranked across the warp
   {
-    const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
-    const float cut = (kth == NEG_INF) ? NEG_INF : kth - margin;
     __shared__ int s_idx[32];
-    __shared__ float s_lg[32], s_b[32];
     int base = 0;
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
       const int e = lane + 32 * i;
-      const bool pred = e < E && key[i] >= cut;
+      const bool pred = e < E && okey[i] >= ocut;
       const unsigned m = __ballot_sync(0xffffffffu, pred);
       const int pos = base + __popc(m & ((1u << lane) - 1u));
-      if (pred && pos < 32) {
-        s_idx[pos] = e;
-        s_lg[pos] = lgt[i];
-        s_b[pos] = b[i];
-      }
+      if (pred && pos < 32) s_idx[pos] = e;
       base += __popc(m);
     }
     __syncwarp();
     if (base <= 32) {
       const bool have = lane < base;
       const int idx = have ? s_idx[lane] : 0x7fffffff;
-      const float sv = have ? sigmoid_exact_f32(s_lg[lane]) : 0.f;
-      float kx = have ? sv + s_b[lane] : NEG_INF;
-      if (isnan(kx)) kx = NEG_INF;
+      float sv = 0.f;
+      const float kx = have ? exact_key(s_lg, s_b, idx, sv) : NEG_INF;
       int rank = 0;
       for (int j = 0; j < 32; ++j) {
         const float kj = __shfl_sync(0xffffffffu, kx, j);
@@ -117,44 +137,9 @@ __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ log
     }
   }
   // general path (more than 32 candidates, e.g. many equal keys): k rounds of
-  // warp arg-max over the exact keys of all candidates
+  // warp arg-max over the exact keys of the candidates not taken yet (exact
+  // keys recomputed each round: this path is rare)
   uint32_t taken = 0;
-  // exact keys for the candidates: each lane evaluates one candidate per
-  // round (all lanes in step)
-  const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
-  const float cut = (kth == NEG_INF) ? NEG_INF : kth - margin;
-  uint32_t cand = 0;
-  float sx[KPL];
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int e = lane + 32 * i;
-    sx[i] = 0.f;
-    if (e < E && key[i] >= cut) cand |= 1u << i;
-  }
-  const uint32_t cand0 = cand;
-  while (__any_sync(0xffffffffu, cand != 0)) {
-    const int pick = cand ? __ffs(cand) - 1 : -1;
-    float lv = 0.f, bv = 0.f;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i)
-      if (i == pick) {
-        lv = lgt[i];
-        bv = b[i];
-      }
-    const float sv = sigmoid_exact_f32(lv);
-    float kx = sv + bv;
-    if (isnan(kx)) kx = NEG_INF;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i)
-      if (i == pick) {
-        sx[i] = sv;
-        key[i] = kx;
-      }
-    if (pick >= 0) cand &= cand - 1;
-  }
-#pragma unroll
-  for (int i = 0; i < KPL; ++i)
-    if (!((cand0 >> i) & 1u)) key[i] = NEG_INF;  // not a candidate: cannot be chosen
   float mys = 0.f;
   int myid = -1;
   double sum = 0.0;
@@ -165,10 +150,14 @@ __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ log
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && e < bi))) {
-        bk = key[i];
-        bi = e;
-        bs = sx[i];
+      if (e < E && okey[i] >= ocut && !((taken >> i) & 1u)) {
+        float sv;
+        const float kx = exact_key(s_lg, s_b, e, sv);
+        if (kx > bk || (kx == bk && e < bi)) {
+          bk = kx;
+          bi = e;
+          bs = sv;
+        }
       }
     }
     warp_argmax(bk, bi);
