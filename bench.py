@@ -77,15 +77,18 @@ def job_throughput(dist, world_size, tokens_per_rank_step, steps, rank_ms, devic
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples during the timed region (200 ms period)."""
+    """nvidia-smi samples (100 ms period), started before the warm-up so that
+    it is running when the timed region begins; only samples stamped inside
+    the timed region [begin(), end()] are kept (the nearest one if none is)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
 
     def start(self):
@@ -93,10 +96,24 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -107,22 +124,34 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((self._stamp(parts[0]), float(parts[2]), float(parts[3]),
+                             {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1]
+        note = None
+        if not inside and rows:
+            mid = 0.5 * (self.t0 + self.t1) if self.t0 is not None and self.t1 is not None else None
+            dated = [r for r in rows if r[0] is not None]
+            if mid is not None and dated:
+                inside = [min(dated, key=lambda r: abs(r[0] - mid))]
+                note = "no sample inside the timed region; nearest sample"
+        sm = [r[1] for r in inside]
+        reasons = set().union(*[r[3] for r in inside]) if inside else set()
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if note:
+            out["note"] = note
+        return out
 
 
 # ----------------------------------------------------------------------------- peaks
@@ -134,15 +163,25 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+FC1_KERNEL_SOURCES = ("gemm_pair.cu", "gemm_dev.cuh", "gemm.cuh", "ptx.cuh")
+
+
+def fc1_kernel_sha256():
+    """sha256 over the sources of the prefill FC1 kernel (in a fixed order)."""
+    h = hashlib.sha256()
+    for f in FC1_KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "mxfp8_mxfp4_moe_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def fc1_traffic_record():
     """DRAM bytes per FC1 launch from a committed ncu summary, if the kernel
-    source it was taken on is unchanged (else null)."""
+    sources it was taken on are unchanged (else null)."""
     path = os.path.join(ROOT, "profiles", "fc1_dram_traffic.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
-    src = open(os.path.join(ROOT, "mxfp8_mxfp4_moe_gb300", "csrc", "gemm.cu"), "rb").read()
-    if rec.get("gemm_cu_sha256") != hashlib.sha256(src).hexdigest():
+    if rec.get("fc1_kernel_sha256") != fc1_kernel_sha256():
         return None
     return rec
 
@@ -198,6 +237,8 @@ class Layer:
 
 def time_layer(layer, steps, warmup, dist, device, clocks=None):
     import torch
+    if clocks:
+        clocks.start()  # running well before the timed region begins
     for _ in range(warmup):
         layer.forward()
     torch.cuda.synchronize()
@@ -208,12 +249,14 @@ def time_layer(layer, steps, warmup, dist, device, clocks=None):
     barrier(dist)
     torch.cuda.synchronize()
     if clocks:
-        clocks.start()
+        clocks.begin()
     start.record(stream)
     for _ in range(steps):
         layer.forward()
     end.record(stream)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.end()
     clk = clocks.stop() if clocks else None
     barrier(dist)
     total_ms = start.elapsed_time(end)
@@ -448,9 +491,24 @@ def run_ours(args):
 
 def run_profile(args):
     """Lean mode for profiler captures: one workload, warm-up + steps forwards,
-    stage times printed as JSON (no clocks, baselines or e2e)."""
+    stage times printed as JSON (no clocks, baselines or e2e).  "route:NAME"
+    runs only the routing kernel on workload NAME's logits (no weights on the
+    device), for multi-pass captures of that kernel."""
     import torch
     torch.cuda.set_device(0)
+    if args.profile.startswith("route:"):
+        import mxfp8_mxfp4_moe_gb300 as K
+        w = W.WORKLOADS[args.profile.split(":", 1)[1]]
+        s = W.gen_small_inputs(w)
+        logits = torch.from_numpy(s["logits"]).cuda()
+        bias = torch.from_numpy(s["bias"]).cuda()
+        ids = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+        wts = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            K.kmoe_route(logits, bias, w.k, ids, wts)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": args.profile, "T": w.T, "E": w.E, "k": w.k}))
+        return 0
     w = {**W.WORKLOADS, **W.PROFILE_WORKLOADS}[args.profile]
     layer = Layer(w, torch.device("cuda", 0))
     for _ in range(args.warmup + args.steps):
