@@ -107,7 +107,10 @@ cudaError_t launch_quant_rows(const void* x, int rows, int cols, int fmt, uint8_
 
 // One block per token.  Threads 0..k-1 first resolve the token's k slots to
 // expert-sorted rows and token tiles; then each thread quantises one
-// 32-element group and writes its 32 code bytes once per routed slot.  The
+// 32-element group.  A warp's 32 groups form one contiguous 1 KB run of code
+// bytes per routed slot: the lanes exchange their codes once (shuffles) so
+// that each store instruction writes 512 contiguous bytes (lane l: 16-byte
+// chunk l, then chunk 32 + l), and the run is stored once per slot.  The
 // four groups of a 128-wide K block sit in an aligned quad of lanes and their
 // scale bytes are adjacent in the token-tile scale layout, so the quad merges
 // them and its first lane writes one 32-bit word per slot.
@@ -138,30 +141,47 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     s_local[j] = local;
   }
   __syncthreads();
+  const int lane = static_cast<int>(threadIdx.x) & 31;
   const int gpr = H / 32;  // a multiple of 4: quads are wholly in or out of range
   const int KB = H / 128;
   for (int g0 = 0; g0 < gpr; g0 += blockDim.x) {
     const int g = g0 + static_cast<int>(threadIdx.x);
-    const bool active = g < gpr;
-    const unsigned mask = __ballot_sync(0xffffffffu, active);
-    if (!active) continue;
-    float v[32];
-    load_group_bf16(x + static_cast<size_t>(t) * H + 32 * g, v);
-    const int e = e4m3_scale_exp(group_amax(v));
-    uint32_t out[8];
-    e4m3_group(v, exp2i(-e), out);
-    const uint4 lo = make_uint4(out[0], out[1], out[2], out[3]);
-    const uint4 hi = make_uint4(out[4], out[5], out[6], out[7]);
-    uint32_t sc = static_cast<uint32_t>(e + 127) << (8 * (g & 3));
-    sc |= __shfl_xor_sync(mask, sc, 1);
-    sc |= __shfl_xor_sync(mask, sc, 2);
+    const int gw = g - lane;                     // first group of this warp's run
+    if (gw >= gpr) continue;                     // the whole warp is past the row
+    const int nact = min(32, gpr - gw);          // groups of the run (a multiple of 4)
+    const bool active = lane < nact;
+    uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int e = 0;
+    if (active) {
+      float v[32];
+      load_group_bf16(x + static_cast<size_t>(t) * H + 32 * g, v);
+      e = e4m3_scale_exp(group_amax(v));
+      e4m3_group(v, exp2i(-e), out);
+    }
+    // chunk c of the run (16 bytes) = half (c & 1) of group c >> 1
+    uint32_t c0[4], c1[4];
+    const int src0 = lane >> 1, src1 = 16 + (lane >> 1);
+    const bool hi = lane & 1;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t a0 = __shfl_sync(0xffffffffu, out[w], src0), a1 = __shfl_sync(0xffffffffu, out[4 + w], src0);
+      const uint32_t b0 = __shfl_sync(0xffffffffu, out[w], src1), b1 = __shfl_sync(0xffffffffu, out[4 + w], src1);
+      c0[w] = hi ? a1 : a0;
+      c1[w] = hi ? b1 : b0;
+    }
+    const uint4 v0 = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+    const uint4 v1 = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+    const bool st0 = src0 < nact, st1 = src1 < nact;
+    uint32_t sc = active ? static_cast<uint32_t>(e + 127) << (8 * (g & 3)) : 0u;
+    sc |= __shfl_xor_sync(0xffffffffu, sc, 1);
+    sc |= __shfl_xor_sync(0xffffffffu, sc, 2);
     for (int j = 0; j < k; ++j) {
       const int row = s_row[j];
       if (row < 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(row) * H + 32 * g);
-      dst[0] = lo;
-      dst[1] = hi;
-      if ((g & 3) == 0)
+      uint4* run = reinterpret_cast<uint4*>(xq + static_cast<size_t>(row) * H + 32 * gw);
+      if (st0) run[lane] = v0;
+      if (st1) run[32 + lane] = v1;
+      if (active && (g & 3) == 0)
         *reinterpret_cast<uint32_t*>(xsf + tile_sf_offset(s_tile[j], s_local[j], g, nch, KB)) = sc;
     }
   }

@@ -22,6 +22,9 @@ TINY_UNSAT = W.WORKLOADS["tiny"].with_(name="tiny_unsaturated", sf_lo=117, sf_hi
 # full and partial tiles; the skewed bias gives experts of 1 to ~1000 rows.
 PAIR_EVEN = W.WORKLOADS["tiny"].with_(name="pair_tiles", T=4096, H=512, I=512, E=32, k=2)
 PAIR_SKEW = PAIR_EVEN.with_(name="pair_tiles_skewed", skewed=True)
+# SiTU with other beta values (the kernels specialise beta = 4)
+TINY_BETA = TINY_UNSAT.with_(name="tiny_beta2_10", situ_beta=2.0, situ_linear_beta=10.0)
+PAIR_BETA = PAIR_EVEN.with_(name="pair_tiles_beta3_20", situ_beta=3.0, situ_linear_beta=20.0, sf_lo=117, sf_hi=121)
 
 
 @pytest.fixture(scope="module")
@@ -66,7 +69,7 @@ def _check_stages(w, p, ws, s, ref, tokens):
     return st
 
 
-@pytest.mark.parametrize("wl", [W.WORKLOADS["tiny"], TINY_UNSAT], ids=["tiny", "tiny_unsaturated"])
+@pytest.mark.parametrize("wl", [W.WORKLOADS["tiny"], TINY_UNSAT, TINY_BETA], ids=["tiny", "tiny_unsaturated", "beta2"])
 def test_forward_tiny_full(K, wl):
     out, ws, p, s, _ = run_forward(wl)
     tokens = np.arange(wl.T)
@@ -75,7 +78,7 @@ def test_forward_tiny_full(K, wl):
     assert_output_parity(out, ref["out"], wl.name)
 
 
-@pytest.mark.parametrize("wl", [PAIR_EVEN, PAIR_SKEW], ids=["even", "skewed"])
+@pytest.mark.parametrize("wl", [PAIR_EVEN, PAIR_SKEW, PAIR_BETA], ids=["even", "skewed", "beta3"])
 def test_forward_pair_tiles_every_token(K, wl):
     out, ws, p, s, _ = run_forward(wl)
     assert K.kmoe_workspace_layout(p).tile_rows == 224
