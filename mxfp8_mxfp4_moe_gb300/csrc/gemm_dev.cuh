@@ -99,12 +99,13 @@ __device__ __forceinline__ int stg_at(int r, int c) { return stg_unit(r, c >> 2)
 // (warp eq of the group reads lane quarter q).
 //   FC2: fp32 stores of rows 128*mt + lane to y of each column's routed slot.
 //   FC1: the group stages the chunk in smem (`stg`, 128 x 32 floats), then
-//        each thread takes 16 consecutive intermediate columns of one token:
+//        each math thread takes 16 consecutive intermediate columns of a token:
 //        SiTU of (gate, up) = (tile rows i, 64 + i), the MXFP8 scale of the
 //        32-group (amax over two threads), E4M3 codes as one 16-byte store.
 template <bool FC1, int NCH>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk, int mt, uint32_t tacc, int c0,
-                                               float* stg, int q, int eq, int lane, int grp) {
+                                               float* stg, int q, int eq, int lane, int grp, int skip_eq = -1,
+                                               int heavy_eq = -1) {
   uint32_t r[32];
   tmem_ld_32x32b_x32(tacc + c0, r);
   tmem_ld_wait();
@@ -129,40 +130,53 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
                       __uint_as_float(r[4 * u + 3]));
   }
   named_barrier(2 + grp, 128);
-  {
-    // thread -> (column, 32-group of the 64 intermediate indices, half)
-    const int t = eq * 32 + lane;
-    const int cl = t >> 2;
-    const int gh = (t >> 1) & 1;
-    const int hh = t & 1;
-    const int col = c0 + cl;
-    const int i0 = 32 * gh + 16 * hh;
-    float act[16];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float g = stg[stg_at(i0 + i, cl)];
-      const float u = stg[stg_at(64 + i0 + i, cl)];
-      act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
-      amax = fmaxf(amax, fabsf(act[i]));
+  // 128 work units = (column, 32-group of the 64 intermediate indices, half),
+  // 16 consecutive intermediate values each; spread over the group's warps
+  // except warp `skip_eq` (the one that shares the MMA warp's scheduler); with
+  // three math warps, warp `heavy_eq` takes the extra pass.  Units u and u ^ 1
+  // (the two halves of a quantisation group) always fall in the same pass of
+  // the same warp.
+  if (eq != skip_eq) {
+    int wm = eq;  // rank among the math warps (0 takes the extra pass)
+    if (skip_eq >= 0) {
+      const int r = eq > skip_eq ? eq - 1 : eq;             // 0..2
+      const int h = heavy_eq > skip_eq ? heavy_eq - 1 : heavy_eq;
+      wm = r == h ? 0 : (r < h ? r + 1 : r);
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the other half of the group
-    const int e = e4m3_scale_exp(amax);
-    const float inv = exp2i(-e);
-    uint32_t w[4];
+    const int stride = skip_eq >= 0 ? 96 : 128;
+    for (int t = wm * 32 + lane; t < 128; t += stride) {
+      const int cl = t >> 2;
+      const int gh = (t >> 1) & 1;
+      const int hh = t & 1;
+      const int col = c0 + cl;
+      const int i0 = 32 * gh + 16 * hh;
+      float act[16];
+      float amax = 0.0f;
 #pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4] * inv, act[4 * k4 + 1] * inv),
-                                                   __NV_SATFINITE, __NV_E4M3);
-      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4 + 2] * inv, act[4 * k4 + 3] * inv),
-                                                   __NV_SATFINITE, __NV_E4M3);
-      w[k4] = (lo & 0xFFFFu) | (hi << 16);
-    }
-    if (col < wk.n) {
-      *reinterpret_cast<uint4*>(a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-      if (hh == 0)
-        a.isf[tile_sf_offset(wk.tile, col, 2 * mt + gh, NCH, a.I / 128)] = static_cast<uint8_t>(e + 127);
+      for (int i = 0; i < 16; ++i) {
+        const float g = stg[stg_at(i0 + i, cl)];
+        const float u = stg[stg_at(64 + i0 + i, cl)];
+        act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
+        amax = fmaxf(amax, fabsf(act[i]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the other half of the group
+      const int e = e4m3_scale_exp(amax);
+      const float inv = exp2i(-e);
+      uint32_t w[4];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4] * inv, act[4 * k4 + 1] * inv),
+                                                     __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4 + 2] * inv, act[4 * k4 + 3] * inv),
+                                                     __NV_SATFINITE, __NV_E4M3);
+        w[k4] = (lo & 0xFFFFu) | (hi << 16);
+      }
+      if (col < wk.n) {
+        *reinterpret_cast<uint4*>(a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+        if (hh == 0)
+          a.isf[tile_sf_offset(wk.tile, col, 2 * mt + gh, NCH, a.I / 128)] = static_cast<uint8_t>(e + 127);
+      }
     }
   }
   named_barrier(2 + grp, 128);

@@ -247,6 +247,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
     const int ew = warp - 2;
     const int grp = ew >> 2;
     const int eq = ew & 3;
+    // Warp w runs on scheduler w % 4: the MMA warp (1) shares one with the
+    // epilogue warp of lane quarter 1, the token producer (PRODB_WARP) with
+    // quarter 2's.  The quarter-1 warp leaves the SiTU math to the other
+    // three, and the extra pass goes to the warp whose scheduler hosts no
+    // other role.
+    constexpr int kMmaSchedEq = (1 + 4 - 2) & 3;
+    constexpr int kHeavyEq = 1;  // warp 3, scheduler 3
+    static_assert(((kHeavyEq + 2) & 3) != (C::PRODB_WARP & 3) && ((kHeavyEq + 2) & 3) != 0 &&
+                      ((kHeavyEq + 2) & 3) != 1,
+                  "the extra SiTU pass goes to a scheduler without a producer or the MMA warp");
     float* stg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE) + grp * C::STG_FLOATS;
     const uint32_t lead_acc_empty = cluster_map(acc_empty, 0);
     uint32_t li = 0;
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::BN;
       const int nchunk = (wk.n + 31) >> 5;
       for (int ci = grp; ci < nchunk; ci += C::NGRP)
-        epilogue_chunk<C::FC1, C::NCH>(a, wk, mt, tacc, ci * 32, stg, q, eq, lane, grp);
+        epilogue_chunk<C::FC1, C::NCH>(a, wk, mt, tacc, ci * 32, stg, q, eq, lane, grp, kMmaSchedEq, kHeavyEq);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
