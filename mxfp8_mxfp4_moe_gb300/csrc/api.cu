@@ -285,7 +285,8 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
 
   auto mark = [&](cudaEvent_t e) { return (ev && e) ? cudaEventRecord(e, stream) : cudaSuccess; };
   KMOE_CK(mark(ev ? ev->start : nullptr));
-  KMOE_CK(cudaMemsetAsync(err, 0, 16, stream));  // the error word reports this call only
+  // the error word reports this call only; words 2 and 3 are the FC1 / FC2 work-item counters
+  KMOE_CK(cudaMemsetAsync(err, 0, 16, stream));
   if (given) {
     KMOE_CK(cudaMemcpyAsync(ids, topk_ids, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
     KMOE_CK(cudaMemcpyAsync(wts, topk_w, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
@@ -304,11 +305,12 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
               L.max_tiles, H, I, iq, isf, static_cast<float>(2.0 / p->situ_beta),
               static_cast<float>(2.0 / p->situ_linear_beta),
               static_cast<float>(static_cast<double>(p->situ_beta) * p->situ_linear_beta), nullptr, slot_of_row,
-              err, kWaitBudgetNs};
+              err, kWaitBudgetNs, reinterpret_cast<int*>(err) + 2};
   KMOE_CK(launch_moe_gemm(true, L.BN, kps1, m1, a1, grid, stream));
   KMOE_CK(mark(ev ? ev->fc1 : nullptr));
   GemmArgs a2{counts, seg_start, tile_start, w2_k, w2_k + weight_blocks(p, 1) * 8192, isf, E, H / 128, I / 128,
-              L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs};
+              L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs,
+              reinterpret_cast<int*>(err) + 3};
   KMOE_CK(launch_moe_gemm(false, L.BN, kps2, m2, a2, grid, stream));
   KMOE_CK(mark(ev ? ev->fc2 : nullptr));
   KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));

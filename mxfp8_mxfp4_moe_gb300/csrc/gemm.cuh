@@ -40,6 +40,7 @@ struct GemmArgs {
   const int32_t* slot_of_row;  // [R]
   uint32_t* err;
   unsigned long long budget_ns;
+  int* sched;  // work-item counter of this launch (zero before it; CTA-pair kernel)
 };
 
 // Re-lays raw codes [E, rows, K/2] and scales [E, rows, K/32] into prepared blocks.

@@ -26,10 +26,11 @@
 
 namespace kmoe {
 
-template <bool FC1_, int STAGES_>
+template <bool FC1_, int STAGES_, bool DYN_>
 struct PairCfg {
   static constexpr bool FC1 = FC1_;
   static constexpr int STAGES = STAGES_;
+  static constexpr bool DYN = DYN_;  // work items claimed dynamically (else pair p takes p, p + npairs, ...)
   static constexpr int KPS = 2;          // 128-wide K blocks per stage (8 pair MMAs)
   static constexpr int BN = 224;         // token rows per item (both CTAs)
   static constexpr int HALF = BN / 2;    // token rows loaded by each CTA
@@ -66,6 +67,8 @@ struct PairCfg {
                 "128-byte-swizzled operands start on 1 KB");
 };
 
+constexpr int kRing = 8;  // work-item ring slots
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __grid_constant__ GemmMaps maps,
                                                                      const GemmArgs a) {
@@ -76,11 +79,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* item_full = done + 1;  // [kRing]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(item_full + kRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // MMA width of item li in item_n[li & 3], written by the token producer
   // before it arrives on the item's first stage (so the MMA thread decodes nothing)
   volatile uint32_t* item_n = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  // work-item ring: index of the pair's li-th item in item_w[li % kRing]
+  volatile int* item_w = reinterpret_cast<volatile int*>(tmem_slot + 6);
   int32_t* tsm = reinterpret_cast<int32_t*>(smem + C::TS_OFF);
   stage_tile_start(a, tsm);
 
@@ -98,6 +104,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       mbar_init(&acc_empty[b], 2 * C::EPI_WARPS);  // epilogue warps of both CTAs
     }
     mbar_init(done, 1);
+    for (int i = 0; i < kRing; ++i) mbar_init(&item_full[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -116,10 +123,28 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
   cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
   const int total = (a.MT / C::NT) * tsm[a.E];
   const uint64_t budget = a.budget_ns;
+  // Work items are claimed dynamically (balance across pairs): the even CTA's
+  // token producer takes them from a global counter, two ahead of its own
+  // progress, and publishes each index to both CTAs' rings (item_full[slot]
+  // completes once per publication); every role reads the same sequence, and
+  // -1 ends it.  A slot is rewritten only kRing publications later, when every
+  // role has long passed it (producers run at most a few stages ahead of the
+  // MMA, the MMA at most two items ahead of the epilogues).
+  // With DYN off the pair takes items p, p + npairs, ... (no ring).
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const bool fetcher = C::DYN && lead && warp == C::PRODB_WARP && lane == 0;
+  auto get_item = [&](uint32_t li) -> int {
+    if (!C::DYN) {
+      const int w = pair + static_cast<int>(li) * npairs;
+      return w < total ? w : -1;
+    }
+    const uint32_t sl = li % kRing;
+    if (!mbar_wait_bounded<true>(&item_full[sl], (li / kRing) & 1u, budget, a.err, abort_flag)) return -1;
+    return item_w[sl];
+  };
 
   if (warp == 0 || warp == C::PRODB_WARP) {
     // ------------------------------------------------------------ producers
@@ -130,9 +155,45 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       const uint64_t pol = is_a ? policy_evict_normal() : policy_evict_last();
       const uint32_t tx2 = 2u * C::KPS * (is_a ? C::A_TX + 512 : C::B_BYTES + C::NCH * 512);
       const uint32_t lead_full = cluster_map(full, 0);
-      uint32_t it = 0, li = 0;
+      uint32_t it = 0;
       bool ok = true;
-      for (int w = pair; w < total && ok; w += npairs, ++li) {
+      // the fetcher's publication state; each claim (atomicAdd) is issued one
+      // item before its value is needed, so its latency overlaps the loads
+      uint32_t published = 0;
+      bool ended = false;
+      int claimed = 0;
+      const uint32_t peer_item_full = cluster_map(item_full, 1);
+      const uint32_t peer_item_w = cluster_map(const_cast<int*>(item_w), 1);
+      auto publish = [&](int w) {
+        if (ended) return;
+        if (w >= total) {
+          w = -1;
+          ended = true;
+        }
+        const uint32_t sl = published % kRing;
+        item_w[sl] = w;
+        st_shared_cluster_u32(peer_item_w + 4u * sl, static_cast<uint32_t>(w));
+        mbar_arrive(&item_full[sl]);                    // release: orders the local store
+        mbar_arrive_remote(peer_item_full + 8u * sl);   // release.cluster: orders the remote store
+        ++published;
+      };
+      if (fetcher) {
+        publish(atomicAdd(a.sched, 1));
+        publish(atomicAdd(a.sched, 1));
+        claimed = atomicAdd(a.sched, 1);
+      }
+      for (uint32_t li = 0; ok; ++li) {
+        int w;
+        if (fetcher) {
+          w = item_w[li % kRing];  // published by this thread
+          if (w >= 0 && !ended) {
+            publish(claimed);      // keep two items published ahead
+            if (!ended) claimed = atomicAdd(a.sched, 1);
+          }
+        } else {
+          w = get_item(li);
+        }
+        if (w < 0) break;
         Work wk;
         decode_work(a, tsm, C::BN, C::NT, w, wk);
         const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
@@ -194,9 +255,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       const uint64_t sfbdesc0 = sdesc_sf_32x16(smem_u32(smem + C::SFB_OFF));
       const uint32_t sf_base = tmem + C::SF_COL0;
       int s = 0;
-      uint32_t ph = 0, li = 0, slot = 0;
+      uint32_t ph = 0, slot = 0;
       bool ok = true;
-      for (int w = pair; w < total && ok; w += npairs, ++li) {
+      for (uint32_t li = 0; ok; ++li) {
+        if (get_item(li) < 0) break;
         const uint32_t acc = li & 1u;
         if (!mbar_wait_bounded<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
@@ -259,8 +321,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
                   "the extra SiTU pass goes to a scheduler without a producer or the MMA warp");
     float* stg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE) + grp * C::STG_FLOATS;
     const uint32_t lead_acc_empty = cluster_map(acc_empty, 0);
-    uint32_t li = 0;
-    for (int w = pair; w < total; w += npairs, ++li) {
+    for (uint32_t li = 0;; ++li) {
+      const int w = get_item(li);
+      if (w < 0) break;
       Work wk;
       decode_work(a, tsm, C::BN, C::NT, w, wk);
       const uint32_t acc = li & 1u;
@@ -336,7 +399,10 @@ bool pair_gemm_supported(int MT, int KB) { return MT % 2 == 0 && KB % 2 == 0; }
 
 cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
   if (!pair_gemm_supported(a.MT, a.KB)) return cudaErrorInvalidValue;
-  return fc1 ? launch_pair<PairCfg<true, 3>>(maps, a, sms, st) : launch_pair<PairCfg<false, 3>>(maps, a, sms, st);
+  // FC1 claims items dynamically (its pairs otherwise finished up to 4 % apart);
+  // FC2's shorter items do better in the fixed order.
+  return fc1 ? launch_pair<PairCfg<true, 3, true>>(maps, a, sms, st)
+             : launch_pair<PairCfg<false, 3, false>>(maps, a, sms, st);
 }
 
 }  // namespace kmoe
