@@ -298,38 +298,59 @@ def mma_peak(device, N=224, iters=500000):
 
 
 def e2e_time(layer, steps, warmup):
-    """Same metric through the C ABI with host buffers: per step the H2D copy of
-    x, logits and bias from pinned memory, the forward, and the D2H read of the
-    output, all inside the timed region."""
+    """Same metric through the C ABI with host buffers: every step copies its
+    x, logits and bias from pinned host memory to the device, runs the
+    forward, and reads its output back to pinned host memory, all inside the
+    timed region.  Two buffer sets and three streams (copy-in, compute,
+    copy-out) let the copies of neighbouring steps overlap a step's compute,
+    as a serving loop would; events order every buffer reuse."""
     import torch
     hx = layer.x.cpu().pin_memory()
     hl = layer.logits.cpu().pin_memory()
     hb = layer.bias.cpu().pin_memory()
-    hout = torch.empty(layer.out.shape, dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty_like(layer.x)
-    dl = torch.empty_like(layer.logits)
-    db = torch.empty_like(layer.bias)
-
-    def step():
-        dx.copy_(hx, non_blocking=True)
-        dl.copy_(hl, non_blocking=True)
-        db.copy_(hb, non_blocking=True)
-        layer.forward(x=dx, logits=dl, bias=db)
-        hout.copy_(layer.out, non_blocking=True)
-
-    for _ in range(warmup):
-        step()
+    hout = [torch.empty(layer.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dx = [torch.empty_like(layer.x) for _ in range(2)]
+    dl = [torch.empty_like(layer.logits) for _ in range(2)]
+    db = [torch.empty_like(layer.bias) for _ in range(2)]
+    dout = [torch.empty_like(layer.out) for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for e in comp_done + out_done:
+        e.record(torch.cuda.current_stream())
     torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        step()
-    e.record()
+
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(comp_done[b])          # step i-2 finished reading dx[b]...
+            dx[b].copy_(hx, non_blocking=True)
+            dl[b].copy_(hl, non_blocking=True)
+            db[b].copy_(hb, non_blocking=True)
+            in_done[b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_done[b])
+            s_comp.wait_event(out_done[b])         # ...and its output was read back
+            layer.forward(x=dx[b], logits=dl[b], bias=db[b], out=dout[b])
+            comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            hout[b].copy_(dout[b], non_blocking=True)
+            out_done[b].record(s_out)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    for i in range(steps):
+        step(warmup + i)
+    end.record(s_out)  # after the last step's read-back
     torch.cuda.synchronize()
     h2d = hx.numel() * 2 + hl.numel() * 4 + hb.numel() * 4
-    d2h = hout.numel() * 2
-    return s.elapsed_time(e), h2d, d2h
+    d2h = hout[0].numel() * 2
+    return start.elapsed_time(end), h2d, d2h
 
 
 # ----------------------------------------------------------------------------- CPU oracle
