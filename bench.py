@@ -459,6 +459,41 @@ def run_ours(args):
     d_layer_bytes = touched * per_expert_all + 2 * wd.T * wd.H * 2 + 4 * wd.T * wd.E
     d_layer_gbs = d_layer_bytes / (d_us / 1e6) / 1e9
 
+    del dl, weights
+    torch.cuda.empty_cache()
+
+    # ---- the real checkpoint's expert shape (3584-wide latent, I=3072): prefill and decode
+    wr = W.NEXT_WORKLOADS["real_prefill"]
+    rl = Layer(wr, device)
+    r_total, _ = time_layer(rl, args.steps, args.warmup, dist, device, None)
+    r_total = reduce_max(dist, r_total, device)
+    r_ms = r_total / args.steps
+    r_stages = time_stages(rl, max(3, min(args.steps, 10)))
+    rl.check()
+    r_weights = rl.weights
+    del rl
+    torch.cuda.empty_cache()
+    wrd = W.NEXT_WORKLOADS["real_decode"]
+    rdl = Layer(wrd, device, weights=r_weights)
+    rd_total, _ = time_layer(rdl, max(args.steps, 20), args.warmup, dist, device, None)
+    rd_total = reduce_max(dist, rd_total, device)
+    rd_us = 1000.0 * rd_total / max(args.steps, 20)
+    rd_touched = rdl.touched_experts()
+    rdl.check()
+    rd_bytes = rd_touched * wrd.expert_weight_bytes() + 2 * wrd.T * wrd.H * 2 + 4 * wrd.T * wrd.E
+    del rdl, r_weights
+    torch.cuda.empty_cache()
+    real_shape = {
+        "workload": "Kimi-K3 real checkpoint expert shape H=3584 I=3072 E=896 top-16",
+        "prefill_T8192": {"ms_per_layer": r_ms, "tokens_per_s": wr.T / (r_ms / 1e3),
+                          "tflops": wr.flops() / (r_ms / 1e3) / 1e12,
+                          "frac_of_fp8_peak": wr.flops() / (r_ms / 1e3) / 1e12 / (2.0 * peaks["bf16_tflops_sustained"]),
+                          "stages_ms": dict(zip(K.STAGE_NAMES, r_stages))},
+        "decode_T16": {"us_per_layer": rd_us, "touched_experts": rd_touched,
+                       "layer_GBs": rd_bytes / (rd_us / 1e6) / 1e9,
+                       "layer_hbm_frac": rd_bytes / (rd_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
+    }
+
     peak_mma = mma_peak(device)
 
     cpu = None
@@ -489,6 +524,7 @@ def run_ours(args):
                          "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
                          "frac_of_measured_mma_roof": fc1_tf / peak_mma["tflops"]},
             "mma_peak_measured": peak_mma,
+            "real_shape": real_shape,
             "decode": {"workload": "Kimi-K3 MoE layer decode T=16 H=7168 I=3584 E=896 top-16",
                        "us_per_layer": d_us, "touched_experts": touched, "layer_GBs": d_layer_gbs,
                        "layer_hbm_frac": d_layer_gbs / peaks["hbm_gbs"],

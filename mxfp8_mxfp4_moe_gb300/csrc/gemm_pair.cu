@@ -44,7 +44,9 @@ struct PairCfg {
   static constexpr int SFA_OFF = B_OFF + KPS * B_BYTES;
   static constexpr int SFB_OFF = SFA_OFF + KPS * 512;
   static constexpr int STAGE = (SFB_OFF + KPS * NCH * 512 + 1023) / 1024 * 1024;
-  static constexpr int EPI_WARPS = 4;  // one per TMEM lane quarter (fewer share the MMA warp's scheduler)
+  // FC1: two groups of four (its SiTU epilogue must stay shorter than a short-K main loop);
+  // FC2: one warp per TMEM lane quarter
+  static constexpr int EPI_WARPS = FC1 ? 8 : 4;
   static constexpr int NGRP = EPI_WARPS / 4;
   static constexpr int PRODB_WARP = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
@@ -399,8 +401,9 @@ bool pair_gemm_supported(int MT, int KB) { return MT % 2 == 0 && KB % 2 == 0; }
 
 cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
   if (!pair_gemm_supported(a.MT, a.KB)) return cudaErrorInvalidValue;
-  // FC1 claims items dynamically (its pairs otherwise finished up to 4 % apart);
-  // FC2's shorter items do better in the fixed order.
+  // FC1 claims items dynamically (in the fixed order its pairs finished up to
+  // 4 % apart at H = 7168, and it is ahead at H = 3584 too); FC2's items do
+  // better in the fixed order.
   return fc1 ? launch_pair<PairCfg<true, 3, true>>(maps, a, sms, st)
              : launch_pair<PairCfg<false, 3, false>>(maps, a, sms, st);
 }

@@ -103,6 +103,43 @@ def test_forward_full_size_sampled(K, name, sample):
     assert torch.isfinite(o).all()
 
 
+@pytest.mark.parametrize("name,sample", [("real_decode", 3), ("real_prefill", 2)])
+def test_forward_real_checkpoint_shape_sampled(K, name, sample):
+    """The real checkpoint's expert shape (3584-wide latent, I = 3072)."""
+    w = W.NEXT_WORKLOADS[name]
+    out, ws, p, s, _ = run_forward(w)
+    rng = np.random.default_rng(321)
+    tokens = np.sort(rng.choice(w.T, size=sample, replace=False))
+    ref = oracle_forward(w, s, tokens)
+    _check_stages(w, p, ws, s, ref, tokens)
+    assert_output_parity(out[torch.from_numpy(tokens).cuda()], ref["out"], name)
+
+
+def test_forward_expert_parallel_local_slice(K):
+    """One rank's slice of an expert-parallel layer: routing over all 896
+    experts, this layer holds 28 of them (global 140..167); slots routed
+    elsewhere are masked (-1) and contribute nothing."""
+    g = W.NEXT_WORKLOADS["real_prefill"].with_(T=2048)
+    s = W.gen_small_inputs(g)
+    ids_g, wts, _ = O.route(s["logits"], s["bias"], g.k)
+    e_loc, off = 28, 140
+    ids = np.where((ids_g >= off) & (ids_g < off + e_loc), ids_g - off, -1).astype(np.int32)
+    wl = g.with_(name="ep_local", E=e_loc)
+    out, ws, p, _, _ = run_forward(wl, small=s, topk_ids=torch.from_numpy(ids).cuda(),
+                                   topk_w=torch.from_numpy(wts.astype(np.float32)).cuda())
+    assert K.kmoe_workspace_layout(p).tile_rows == 224
+    o = out.float().cpu().numpy()
+    none_local = np.all(ids < 0, axis=1)
+    assert none_local.any() and np.all(o[none_local] == 0.0)
+    rng = np.random.default_rng(99)
+    local_tokens = np.flatnonzero(~none_local)
+    tokens = np.sort(rng.choice(local_tokens, size=4, replace=False))
+    used = sorted(set(int(e) for e in ids[tokens].ravel() if e >= 0))
+    ref = O.forward(wl, s["x"], None, None, W.gen_expert_weights_np(wl, used), experts_host=used, tokens=tokens,
+                    ids=ids, topk_w=wts.astype(np.float32).astype(np.float64))
+    assert_output_parity(out[torch.from_numpy(tokens).cuda()], ref["out"], "ep_local")
+
+
 def test_determinism_and_graph_replay(K):
     for name in ("tiny", "reduced"):
         w = W.WORKLOADS[name]

@@ -83,6 +83,14 @@ WORKLOADS = {
     "skewed": Workload("skewed", T=2048, H=7168, I=3584, E=896, k=16, skewed=True),
 }
 
+# The real Kimi-K3 checkpoint runs its routed experts in a 3584-wide latent
+# with I = 3072 (SM120 FlashInfer MXFP4 page, real checkpoint contract); same
+# input distributions.
+NEXT_WORKLOADS = {
+    "real_prefill": Workload("real_prefill", T=8192, H=3584, I=3072, E=896, k=16),
+    "real_decode": Workload("real_decode", T=16, H=3584, I=3072, E=896, k=16),
+}
+
 # Smaller cases of the same kernels, sized for profiler captures (a few GB on
 # the device, still larger than L2): a prefill-like layer with hundreds of rows
 # per touched expert, and a decode-like layer with one or two.
