@@ -20,6 +20,8 @@ Steps and the passages they follow
               gate' = beta*tanh(gate/beta)*sigmoid(gate),
               up'   = beta_lin*tanh(up/beta_lin), out = gate'*up'
               with beta = situ_beta = 4, beta_lin = situ_linear_beta = 25.
+   control    the SwiGLU control activation the SM120 page's kernel runs
+              (alpha 1.702, beta 1, limit 7), in its clamped form (below).
 5. requant    the FC2 input is MXFP8 like the FC1 input (both GEMMs are
               MXFP8 activation x MXFP4 weight, SM120 page, "Goal").
 6. FC2        w2 is [E, H, I/2] packed E2M1 with [E, H, I/32] scales.
@@ -34,6 +36,9 @@ Readings where the pages leave a step open
   DeepSeek-V3-style grouped top-k but give no group counts).
 - the gated-width rule: FC1 must be exactly twice as wide as FC2's K
   ("256 vs 128" at H = I = 128 is the pages' rejected shape).
+- SwiGLU control: the pages give only its parameters; read as the clamped
+  form out = g' * sigmoid(alpha*g') * (u' + beta), g' = min(g, limit),
+  u' = clamp(u, -limit, limit).
 """
 from __future__ import annotations
 
@@ -79,6 +84,24 @@ def situ(gate: np.ndarray, up: np.ndarray, beta: float = 4.0, beta_lin: float = 
     u = np.asarray(up, dtype=np.float64)
     sig = 1.0 / (1.0 + np.exp(-np.clip(g, -700.0, 700.0)))
     return beta * np.tanh(g / beta) * sig * (beta_lin * np.tanh(u / beta_lin))
+
+
+def swiglu(gate: np.ndarray, up: np.ndarray, alpha: float = 1.702, beta: float = 1.0,
+           limit: float = 7.0) -> np.ndarray:
+    """The clamped SwiGLU control activation (SM120 page, activation table:
+    alpha = 1.702, beta = 1, limit = 7): g' = min(g, limit),
+    u' = clamp(u, -limit, limit), out = g' * sigmoid(alpha * g') * (u' + beta)."""
+    g = np.minimum(np.asarray(gate, dtype=np.float64), limit)
+    u = np.clip(np.asarray(up, dtype=np.float64), -limit, limit)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-alpha * g)) * (u + beta)
+
+
+def activation(w, gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """The FC1 activation the workload names (SiTU unless it says "swiglu")."""
+    if getattr(w, "activation", "situ") == "swiglu":
+        return swiglu(gate, up, w.swiglu_alpha, w.swiglu_beta, w.swiglu_limit)
+    return situ(gate, up, w.situ_beta, w.situ_linear_beta)
 
 
 def check_shapes(H: int, I: int, w13: np.ndarray, w2: np.ndarray):
@@ -154,7 +177,7 @@ def forward(w, x_bits, logits, bias, wts, experts_host=None, tokens=None,
         ti, tj = np.nonzero(sub_ids == e)
         we = pos[int(e)] if pos is not None else int(e)
         gate, up = expert_fc1(xq[ti], xs[ti], wts["w13"][we], wts["w13_sf"][we], I)
-        act = situ(gate, up, w.situ_beta, w.situ_linear_beta)
+        act = activation(w, gate, up)
         q, s = F.quantize_mx(act, "e4m3")
         iq[ti, tj] = q
         isf[ti, tj] = s

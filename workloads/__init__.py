@@ -53,6 +53,10 @@ class Workload:
     skewed: bool = False
     situ_beta: float = 4.0
     situ_linear_beta: float = 25.0
+    activation: str = "situ"  # or "swiglu": the clamped SwiGLU control below
+    swiglu_alpha: float = 1.702
+    swiglu_beta: float = 1.0
+    swiglu_limit: float = 7.0
     routed_scaling_factor: float = 1.0
     sf_lo: int = 121  # UE8M0 byte range of the weight scales: 2^-6 .. 2^0
     sf_hi: int = 127
