@@ -31,6 +31,21 @@ E4M3_MAX = 448.0
 E2M1_MAX = 6.0
 
 
+def bf16_decode(bits) -> np.ndarray:
+    """bfloat16 bit patterns -> float64, from the format's definition: sign bit
+    15, 8 exponent bits (bias 127), 7 fraction bits; exponent 0 is subnormal
+    (2^-126 * f/128), exponent 255 is Inf (f = 0) or NaN."""
+    b = np.asarray(bits).astype(np.uint16).astype(np.int64)
+    sign = np.where((b >> 15) & 1, -1.0, 1.0)
+    ex = (b >> 7) & 0xFF
+    fr = (b & 0x7F).astype(np.float64)
+    normal = np.ldexp(1.0 + fr / 128.0, (ex - 127).astype(np.int64))
+    sub = np.ldexp(fr / 128.0, -126)
+    v = np.where(ex == 0, sub, normal)
+    v = np.where(ex == 255, np.where(fr == 0, np.inf, np.nan), v)
+    return sign * v
+
+
 def e2m1_lut() -> np.ndarray:
     """Value of each of the 16 E2M1 codes (1 sign, 2 exponent (bias 1), 1 mantissa bit)."""
     out = np.empty(16, dtype=np.float64)

@@ -4,6 +4,11 @@ TEST INFRASTRUCTURE ONLY: imported by tests, by the smoke check and by the
 CPU-baseline leg of the benchmark; the product path never uses it.
 
 Steps and the passages they follow
+0. router     Kimi-K3 SM120 FlashInfer MXFP4 page, "Phase 1: serving call
+              chain": the TopK step consumes the router's logits, i.e. the
+              gate's dense product of the bf16 hidden state with the bf16
+              gate weight [E, H]; read as the exact dot products rounded
+              once to fp32.
 1. route      Kimi-K3 SM120 FlashInfer MXFP4 page, "Phase 1: serving call
               chain" and its source table (topk.py row): sigmoid scores, the
               e_score_correction_bias takes part only in choosing experts,
@@ -57,6 +62,17 @@ def sigmoid_fp32(logits: np.ndarray) -> np.ndarray:
     with np.errstate(over="ignore"):
         s = 1.0 / (1.0 + np.exp(-x))
     return s.astype(np.float32)
+
+
+def router_logits(x_bits: np.ndarray, wg_bits: np.ndarray) -> np.ndarray:
+    """Router GEMM: logits fp32 [T, E] = fp32(x @ W_g^T) with x bf16 [T, H] and
+    W_g bf16 [E, H] given as bit patterns; the dot products are taken in
+    double (every bf16 product is exact there) and rounded once to fp32."""
+    x = F.bf16_decode(x_bits)
+    g = F.bf16_decode(wg_bits)
+    if x.shape[-1] != g.shape[-1]:
+        raise ShapeError(f"hidden size {x.shape[-1]} != gate weight width {g.shape[-1]}")
+    return (x @ g.T).astype(np.float32)
 
 
 def route(logits: np.ndarray, bias: np.ndarray, k: int):
