@@ -199,7 +199,7 @@ class Layer:
         self.x = torch.from_numpy(s["x"].view(np.int16)).view(torch.bfloat16).to(device)
         self.logits = torch.from_numpy(s["logits"]).to(device)
         self.bias = torch.from_numpy(s["bias"]).to(device)
-        self.p = K.make_params(w.T, w.H, w.I, w.E, w.k, w.situ_beta, w.situ_linear_beta, w.routed_scaling_factor)
+        self.p = layer_params(K, w)
         if weights is None:
             wts = W.gen_expert_weights_torch(w, device)
             w13_k, w2_k = K.kmoe_prepare_weights(self.p, wts["w13"], wts["w13_sf"], wts["w2"], wts["w2_sf"])
@@ -459,7 +459,24 @@ def run_ours(args):
     d_layer_bytes = touched * per_expert_all + 2 * wd.T * wd.H * 2 + 4 * wd.T * wd.E
     d_layer_gbs = d_layer_bytes / (d_us / 1e6) / 1e9
 
-    del dl, weights
+    del dl
+
+    # ---- the SwiGLU control activation on the same prefill layer (same weights)
+    wsg = wp.with_(name="prefill_swiglu", activation="swiglu")
+    sl = Layer(wsg, device, weights=weights)
+    sg_total, _ = time_layer(sl, args.steps, args.warmup, dist, device, None)
+    sg_total = reduce_max(dist, sg_total, device)
+    sg_ms = sg_total / args.steps
+    sg_stages = time_stages(sl, max(3, min(args.steps, 10)))
+    sl.check()
+    swiglu_control = {
+        "workload": "Kimi-K3 MoE layer prefill chunk T=8192 H=7168 I=3584 E=896 top-16, clamped SwiGLU "
+                    f"(alpha {wsg.swiglu_alpha}, beta {wsg.swiglu_beta}, limit {wsg.swiglu_limit}) in place of SiTU",
+        "ms_per_layer": sg_ms, "tokens_per_s": wsg.T / (sg_ms / 1e3),
+        "tflops": wsg.flops() / (sg_ms / 1e3) / 1e12,
+        "stages_ms": dict(zip(K.STAGE_NAMES, sg_stages)),
+    }
+    del sl, weights
     torch.cuda.empty_cache()
 
     # ---- the real checkpoint's expert shape (3584-wide latent, I=3072): prefill and decode
@@ -525,6 +542,7 @@ def run_ours(args):
                          "frac_of_measured_mma_roof": fc1_tf / peak_mma["tflops"]},
             "mma_peak_measured": peak_mma,
             "real_shape": real_shape,
+            "swiglu_control": swiglu_control,
             "decode": {"workload": "Kimi-K3 MoE layer decode T=16 H=7168 I=3584 E=896 top-16",
                        "us_per_layer": d_us, "touched_experts": touched, "layer_GBs": d_layer_gbs,
                        "layer_hbm_frac": d_layer_gbs / peaks["hbm_gbs"],
@@ -580,7 +598,9 @@ def run_profile(args):
 
 
 def layer_params(K, w):
-    return K.make_params(w.T, w.H, w.I, w.E, w.k, w.situ_beta, w.situ_linear_beta, w.routed_scaling_factor)
+    return K.make_params(w.T, w.H, w.I, w.E, w.k, w.situ_beta, w.situ_linear_beta, w.routed_scaling_factor,
+                         activation=w.activation, swiglu_alpha=w.swiglu_alpha, swiglu_beta=w.swiglu_beta,
+                         swiglu_limit=w.swiglu_limit)
 
 
 def main(argv=None):

@@ -66,6 +66,14 @@ enum kmoe_mx_format {
   KMOE_MXFP4_E2M1 = 1   /* two E2M1 codes per byte, element 2j in the low nibble */
 };
 
+/* kmoe_params.flags: the FC1 activation is the clamped SwiGLU control
+ * (SM120 page, activation table: the kernel the pages compare SiTU against)
+ *   out = g' * sigmoid(alpha * g') * (u' + beta),  g' = min(g, limit),
+ *   u' = clamp(u, -limit, limit),
+ * with alpha, beta, limit = swiglu_alpha, swiglu_beta, swiglu_limit; without
+ * the flag it is SiTU (situ_beta, situ_linear_beta). */
+#define KMOE_FLAG_SWIGLU 1u
+
 /* Layer parameters (host struct). */
 typedef struct kmoe_params {
   int T;                        /* tokens, >= 0 */
@@ -73,10 +81,13 @@ typedef struct kmoe_params {
   int I;                        /* expert intermediate size, multiple of 128 */
   int E;                        /* experts, 1..1024 */
   int k;                        /* experts per token, 1..min(E, 32) */
-  float situ_beta;              /* SiTU gate beta (Kimi-K3: 4.0) */
-  float situ_linear_beta;       /* SiTU linear beta (Kimi-K3: 25.0) */
+  float situ_beta;              /* SiTU gate beta (Kimi-K3: 4.0), > 0 */
+  float situ_linear_beta;       /* SiTU linear beta (Kimi-K3: 25.0), > 0 */
   float routed_scaling_factor;  /* applied in the combine (1.0 in the workloads) */
-  uint32_t flags;               /* reserved, must be 0 */
+  uint32_t flags;               /* 0 or KMOE_FLAG_SWIGLU */
+  float swiglu_alpha;           /* SwiGLU control (1.702); used with KMOE_FLAG_SWIGLU */
+  float swiglu_beta;            /* (1.0) */
+  float swiglu_limit;           /* (7.0), > 0 */
 } kmoe_params;
 
 /* Human-readable name of a status code (static string). */

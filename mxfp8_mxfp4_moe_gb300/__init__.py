@@ -33,7 +33,8 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 class kmoe_params(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("situ_beta", ctypes.c_float), ("situ_linear_beta", ctypes.c_float),
-                ("routed_scaling_factor", ctypes.c_float), ("flags", ctypes.c_uint32)]
+                ("routed_scaling_factor", ctypes.c_float), ("flags", ctypes.c_uint32),
+                ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float), ("swiglu_limit", ctypes.c_float)]
 
 
 class kmoe_ws_layout(ctypes.Structure):
@@ -125,8 +126,17 @@ def _dev(t, name, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
-def make_params(T, H, I, E, k, situ_beta=4.0, situ_linear_beta=25.0, routed_scaling_factor=1.0):
-    return kmoe_params(T, H, I, E, k, situ_beta, situ_linear_beta, routed_scaling_factor, 0)
+KMOE_FLAG_SWIGLU = 1
+
+
+def make_params(T, H, I, E, k, situ_beta=4.0, situ_linear_beta=25.0, routed_scaling_factor=1.0,
+                activation="situ", swiglu_alpha=1.702, swiglu_beta=1.0, swiglu_limit=7.0):
+    """`activation` is "situ" (the layer's) or "swiglu" (the clamped SwiGLU control)."""
+    if activation not in ("situ", "swiglu"):
+        raise ValueError(f"activation must be 'situ' or 'swiglu', got {activation!r}")
+    flags = KMOE_FLAG_SWIGLU if activation == "swiglu" else 0
+    return kmoe_params(T, H, I, E, k, situ_beta, situ_linear_beta, routed_scaling_factor, flags,
+                       swiglu_alpha, swiglu_beta, swiglu_limit)
 
 
 def kmoe_status_string(status: int) -> str:

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -86,7 +87,17 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int check_params(const kmoe_params* p) {
   if (!p) return KMOE_ERR_ARG;
-  if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->k <= 0 || p->flags != 0) return KMOE_ERR_ARG;
+  if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->k <= 0) return KMOE_ERR_ARG;
+  if ((p->flags & ~KMOE_FLAG_SWIGLU) != 0u) return KMOE_ERR_ARG;
+  if (p->flags & KMOE_FLAG_SWIGLU) {
+    // finite parameters and a positive clamp
+    if (!std::isfinite(p->swiglu_alpha) || !std::isfinite(p->swiglu_beta) || !std::isfinite(p->swiglu_limit) ||
+        !(p->swiglu_limit > 0.f))
+      return KMOE_ERR_ARG;
+  } else if (!(p->situ_beta > 0.f) || !(p->situ_linear_beta > 0.f) || !std::isfinite(p->situ_beta) ||
+             !std::isfinite(p->situ_linear_beta)) {
+    return KMOE_ERR_ARG;
+  }
   if (p->E > kMaxE || p->k > p->E || p->k > kMaxK) return KMOE_ERR_ARG;
   if (p->H % 128 != 0 || p->I % 128 != 0) return KMOE_ERR_SHAPE;
   // row indices of the weight tensor maps stay within int range
@@ -305,12 +316,13 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
               L.max_tiles, H, I, iq, isf, static_cast<float>(2.0 / p->situ_beta),
               static_cast<float>(2.0 / p->situ_linear_beta),
               static_cast<float>(static_cast<double>(p->situ_beta) * p->situ_linear_beta), nullptr, slot_of_row,
-              err, kWaitBudgetNs, reinterpret_cast<int*>(err) + 2};
+              err, kWaitBudgetNs, reinterpret_cast<int*>(err) + 2,
+              (p->flags & KMOE_FLAG_SWIGLU) ? 1 : 0, p->swiglu_alpha, p->swiglu_beta, p->swiglu_limit};
   KMOE_CK(launch_moe_gemm(true, L.BN, kps1, m1, a1, grid, stream));
   KMOE_CK(mark(ev ? ev->fc1 : nullptr));
   GemmArgs a2{counts, seg_start, tile_start, w2_k, w2_k + weight_blocks(p, 1) * 8192, isf, E, H / 128, I / 128,
               L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs,
-              reinterpret_cast<int*>(err) + 3};
+              reinterpret_cast<int*>(err) + 3, 0, 0.f, 0.f, 0.f};
   KMOE_CK(launch_moe_gemm(false, L.BN, kps2, m2, a2, grid, stream));
   KMOE_CK(mark(ev ? ev->fc2 : nullptr));
   KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));

@@ -41,6 +41,9 @@ struct GemmArgs {
   uint32_t* err;
   unsigned long long budget_ns;
   int* sched;  // work-item counter of this launch (zero before it; CTA-pair kernel)
+  // FC1 activation: 0 = SiTU (kg, ku, bb above), 1 = the clamped SwiGLU control
+  int act;
+  float sw_alpha, sw_beta, sw_limit;
 };
 
 // Re-lays raw codes [E, rows, K/2] and scales [E, rows, K/32] into prepared blocks.

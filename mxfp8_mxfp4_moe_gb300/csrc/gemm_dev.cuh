@@ -1,6 +1,6 @@
 // Device pieces shared by the one-CTA and the CTA-pair expert GEMM kernels:
-// work-item decoding, the SiTU activation and the epilogue of one 32-column
-// accumulator chunk.
+// work-item decoding, the SiTU activation (and the SwiGLU control) and the
+// epilogue of one 32-column accumulator chunk.
 #pragma once
 #include <cuda_fp8.h>
 
@@ -85,6 +85,18 @@ __device__ __forceinline__ float situ_f32(float g, float u, float kg, float ku, 
   return ((g < 0.0f) != (u < 0.0f)) ? -mag : mag;
 }
 
+// The clamped SwiGLU control: g' = min(g, limit), u' = clamp(u, -limit,
+// limit), out = g' * sigmoid(alpha*g') * (u' + beta), the sigmoid from the
+// exponential of a non-positive argument (1/(1+e) or e/(1+e), e = exp(-|z|)).
+__device__ __forceinline__ float swiglu_f32(float g, float u, float alpha, float beta, float limit) {
+  const float gc = fminf(g, limit);
+  const float uc = fminf(fmaxf(u, -limit), limit);
+  const float z = alpha * gc;
+  const float e = __expf(-fabsf(z));
+  const float sig = __fdividef(z >= 0.0f ? 1.0f : e, 1.0f + e);
+  return gc * sig * (uc + beta);
+}
+
 // Epilogue staging tile: 128 rows x 32 floats, unpadded.  The 16-byte unit u
 // of row r is stored at unit u ^ (r & 7) ^ ((r >> 4) & 3), which keeps both
 // the row-wise float4 writes and the column reads of the SiTU step at most
@@ -100,8 +112,9 @@ __device__ __forceinline__ int stg_at(int r, int c) { return stg_unit(r, c >> 2)
 //   FC2: fp32 stores of rows 128*mt + lane to y of each column's routed slot.
 //   FC1: the group stages the chunk in smem (`stg`, 128 x 32 floats), then
 //        each math thread takes 16 consecutive intermediate columns of a token:
-//        SiTU of (gate, up) = (tile rows i, 64 + i), the MXFP8 scale of the
-//        32-group (amax over two threads), E4M3 codes as one 16-byte store.
+//        the activation (SiTU, or the SwiGLU control when a.act is set) of
+//        (gate, up) = (tile rows i, 64 + i), the MXFP8 scale of the 32-group
+//        (amax over two threads), E4M3 codes as one 16-byte store.
 template <bool FC1, int NCH>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk, int mt, uint32_t tacc, int c0,
                                                float* stg, int q, int eq, int lane, int grp, int skip_eq = -1,
@@ -152,12 +165,22 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
       const int i0 = 32 * gh + 16 * hh;
       float act[16];
       float amax = 0.0f;
+      if (a.act == 0) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float g = stg[stg_at(i0 + i, cl)];
-        const float u = stg[stg_at(64 + i0 + i, cl)];
-        act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
-        amax = fmaxf(amax, fabsf(act[i]));
+        for (int i = 0; i < 16; ++i) {
+          const float g = stg[stg_at(i0 + i, cl)];
+          const float u = stg[stg_at(64 + i0 + i, cl)];
+          act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
+          amax = fmaxf(amax, fabsf(act[i]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float g = stg[stg_at(i0 + i, cl)];
+          const float u = stg[stg_at(64 + i0 + i, cl)];
+          act[i] = swiglu_f32(g, u, a.sw_alpha, a.sw_beta, a.sw_limit);
+          amax = fmaxf(amax, fabsf(act[i]));
+        }
       }
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the other half of the group
       const int e = e4m3_scale_exp(amax);

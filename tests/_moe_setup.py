@@ -35,7 +35,8 @@ def device_weights(w: W.Workload, device="cuda"):
 def params(w: W.Workload, **kw):
     import mxfp8_mxfp4_moe_gb300 as K
     d = dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, situ_beta=w.situ_beta, situ_linear_beta=w.situ_linear_beta,
-             routed_scaling_factor=w.routed_scaling_factor)
+             routed_scaling_factor=w.routed_scaling_factor, activation=w.activation,
+             swiglu_alpha=w.swiglu_alpha, swiglu_beta=w.swiglu_beta, swiglu_limit=w.swiglu_limit)
     d.update(kw)
     return K.make_params(**d)
 

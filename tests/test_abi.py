@@ -49,7 +49,17 @@ def test_host_side_argument_errors(K):
     bad = [K.make_params(16, 100, 128, 8, 2),      # H not a multiple of 128
            K.make_params(16, 128, 96, 8, 2),       # I not a multiple of 128
            K.make_params(16, 128, 128, 8, 9),      # k > E
-           K.make_params(-1, 128, 128, 8, 2)]
+           K.make_params(-1, 128, 128, 8, 2),
+           K.make_params(16, 128, 128, 8, 2, situ_beta=0.0),                          # SiTU beta not > 0
+           K.make_params(16, 128, 128, 8, 2, activation="swiglu", swiglu_limit=0.0),  # clamp not > 0
+           K.make_params(16, 128, 128, 8, 2, activation="swiglu", swiglu_alpha=float("inf")),
+           K.make_params(16, 128, 128, 8, 2, activation="swiglu", swiglu_beta=float("nan"))]
+    p_flag = K.make_params(16, 128, 128, 8, 2)
+    p_flag.flags = 2                                                                   # unknown flag bit
+    bad.append(p_flag)
+    assert K.kmoe_workspace_size(K.make_params(16, 128, 128, 8, 2, activation="swiglu")) > 0
+    with pytest.raises(ValueError):
+        K.make_params(16, 128, 128, 8, 2, activation="gelu")
     for p in bad:
         assert K.kmoe_workspace_size(p) == 0
         st = lib.kmoe_forward(ctypes.byref(p), None, None, None, None, None, None, None, None, None, 0, None)

@@ -26,6 +26,14 @@ PAIR_SKEW = PAIR_EVEN.with_(name="pair_tiles_skewed", skewed=True)
 TINY_BETA = TINY_UNSAT.with_(name="tiny_beta2_10", situ_beta=2.0, situ_linear_beta=10.0)
 PAIR_BETA = PAIR_EVEN.with_(name="pair_tiles_beta3_20", situ_beta=3.0, situ_linear_beta=20.0, sf_lo=117, sf_hi=121)
 
+# the clamped SwiGLU control in place of SiTU: with the default weight scales
+# about half the gate/up values pass the clamp (|v| > 7), with the narrow ones
+# none do; the pair case mixes both; one case with other parameters
+TINY_SWIGLU = W.WORKLOADS["tiny"].with_(name="tiny_swiglu", activation="swiglu")
+TINY_SWIGLU_UNSAT = TINY_UNSAT.with_(name="tiny_swiglu_unclamped", activation="swiglu")
+TINY_SWIGLU_P = TINY_SWIGLU.with_(name="tiny_swiglu_a1_b05_l3", swiglu_alpha=1.0, swiglu_beta=0.5, swiglu_limit=3.0)
+PAIR_SWIGLU = PAIR_EVEN.with_(name="pair_tiles_swiglu", activation="swiglu", sf_lo=119, sf_hi=124)
+
 
 @pytest.fixture(scope="module")
 def K():
@@ -69,7 +77,8 @@ def _check_stages(w, p, ws, s, ref, tokens):
     return st
 
 
-@pytest.mark.parametrize("wl", [W.WORKLOADS["tiny"], TINY_UNSAT, TINY_BETA], ids=["tiny", "tiny_unsaturated", "beta2"])
+@pytest.mark.parametrize("wl", [W.WORKLOADS["tiny"], TINY_UNSAT, TINY_BETA, TINY_SWIGLU, TINY_SWIGLU_UNSAT, TINY_SWIGLU_P],
+                         ids=["tiny", "tiny_unsaturated", "beta2", "swiglu", "swiglu_unclamped", "swiglu_params"])
 def test_forward_tiny_full(K, wl):
     out, ws, p, s, _ = run_forward(wl)
     tokens = np.arange(wl.T)
@@ -78,7 +87,7 @@ def test_forward_tiny_full(K, wl):
     assert_output_parity(out, ref["out"], wl.name)
 
 
-@pytest.mark.parametrize("wl", [PAIR_EVEN, PAIR_SKEW, PAIR_BETA], ids=["even", "skewed", "beta3"])
+@pytest.mark.parametrize("wl", [PAIR_EVEN, PAIR_SKEW, PAIR_BETA, PAIR_SWIGLU], ids=["even", "skewed", "beta3", "swiglu"])
 def test_forward_pair_tiles_every_token(K, wl):
     out, ws, p, s, _ = run_forward(wl)
     assert K.kmoe_workspace_layout(p).tile_rows == 224
@@ -113,6 +122,19 @@ def test_forward_real_checkpoint_shape_sampled(K, name, sample):
     ref = oracle_forward(w, s, tokens)
     _check_stages(w, p, ws, s, ref, tokens)
     assert_output_parity(out[torch.from_numpy(tokens).cuda()], ref["out"], name)
+
+
+@pytest.mark.parametrize("name,sample", [("decode", 3), ("prefill", 2)])
+def test_forward_swiglu_control_full_size_sampled(K, name, sample):
+    """The SwiGLU control activation at the full layer sizes."""
+    w = W.WORKLOADS[name].with_(name=name + "_swiglu", activation="swiglu")
+    out, ws, p, s, _ = run_forward(w)
+    assert p.flags == K.KMOE_FLAG_SWIGLU
+    rng = np.random.default_rng(77)
+    tokens = np.sort(rng.choice(w.T, size=sample, replace=False))
+    ref = oracle_forward(w, s, tokens)
+    _check_stages(w, p, ws, s, ref, tokens)
+    assert_output_parity(out[torch.from_numpy(tokens).cuda()], ref["out"], w.name)
 
 
 def test_forward_expert_parallel_local_slice(K):
