@@ -121,6 +121,7 @@ typedef struct kmoe_ws_layout {
   int tile_rows;       /* rows per token tile (BN) chosen for these parameters */
   int max_tiles;       /* capacity of the tile-layout scale arrays, in tiles */
   size_t total;        /* == kmoe_workspace_size(p) */
+  size_t logits;       /* float [T, E] router logits (written by kmoe_forward_router) */
 } kmoe_ws_layout;
 int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out /* host */);
 
@@ -134,6 +135,29 @@ int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out /* host */);
  *   topk_w [T, k] float (out).  E <= 1024, k <= min(E, 32). */
 int kmoe_route(const float* logits, const float* bias, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                cudaStream_t stream);
+
+/* The router (Kimi-K3 SM120 FlashInfer MXFP4 page, "Phase 1: serving call
+ * chain": TopK consumes the gate's logits), fused: the gate GEMM
+ *   logits[t, e] = sum_h x[t, h] * w_gate[e, h]
+ * on the tensor cores (bf16 x bf16, fp32 accumulation, a fixed summation
+ * order for a given (T, H, E)), followed in the same kernel by the routing of
+ * kmoe_route on those logits; tokens of finished 128-token tiles are routed
+ * while the gate GEMM of later tiles runs.
+ *   x [T, H] bf16 and w_gate [E, H] bf16 (both row-major, 16-byte aligned),
+ *   bias [E] float; logits [T, E] float (out, 16-byte aligned), topk_ids
+ *   [T, k] int32 (out), topk_w [T, k] float (out).  H a multiple of 64, E a
+ *   multiple of 4 and <= 1024, k <= min(E, 32).
+ *   workspace: device memory of kmoe_router_workspace_size(T) bytes, 256-byte
+ *   aligned, caller-owned; its first word is the device error word (read it
+ *   with kmoe_device_error).  The call launches one CTA per SM as a
+ *   cooperative launch (all co-resident), so it fails with KMOE_ERR_CUDA if
+ *   the device cannot host them all at once.  Every device wait is bounded;
+ *   a token whose logits did not arrive in time is left masked (ids -1,
+ *   weights 0) and the timeout bit is set. */
+size_t kmoe_router_workspace_size(int T);
+int kmoe_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, int T, int H, int E, int k,
+                float* logits, int32_t* topk_ids, float* topk_w, void* workspace, size_t ws_bytes,
+                cudaStream_t stream);
 
 /* Microscaling quantisation of bf16 rows, one UE8M0 scale per 32 columns.
  * Scale byte = e + 127 with e the smallest integer such that
@@ -199,6 +223,16 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
                     const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
                     void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream,
                     const kmoe_stage_events* ev /* host */);
+
+/* kmoe_forward with the fused router (kmoe_router) in place of the routing
+ * kernel: the routing comes from x and the gate weight w_gate [E, H] bf16
+ * (16-byte aligned; H a multiple of 64, E a multiple of 4) instead of given
+ * logits.  The logits are left in the workspace (kmoe_ws_layout.logits).
+ * Other arguments, the workspace and the error behaviour are those of
+ * kmoe_forward_ex (ev may be null; its `routed` event follows the router). */
+int kmoe_forward_router(const kmoe_params* p, const void* x_bf16, const void* w_gate_bf16, const float* bias,
+                        const uint8_t* w13_k, const uint8_t* w2_k, void* out_bf16, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream, const kmoe_stage_events* ev /* host */);
 
 /* Reads the device error word of `workspace` (synchronises `stream`), clears
  * it, and returns KMOE_OK, KMOE_ERR_TIMEOUT or KMOE_ERR_DEVICE.  *word (host,

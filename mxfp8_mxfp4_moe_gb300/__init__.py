@@ -26,7 +26,8 @@ KMOE_MXFP4_E2M1 = 1
 EXPORTS = ("kmoe_status_string", "kmoe_check_device", "kmoe_workspace_size", "kmoe_workspace_layout",
            "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_weight_bytes", "kmoe_prepare_weights",
            "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error", "kmoe_tile_sf_offset",
-           "kmoe_selftest_wait_timeout", "kmoe_forward_noalloc", "kmoe_mma_peak_run")
+           "kmoe_selftest_wait_timeout", "kmoe_forward_noalloc", "kmoe_mma_peak_run",
+           "kmoe_router_workspace_size", "kmoe_router", "kmoe_forward_router")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -40,7 +41,8 @@ class kmoe_params(ctypes.Structure):
 class kmoe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("err", "topk_ids", "topk_w", "counts", "seg_start", "tile_start",
                                                "row_of_slot", "slot_of_row", "xq", "xsf", "iq", "isf", "y")] + \
-               [("tile_rows", ctypes.c_int), ("max_tiles", ctypes.c_int), ("total", ctypes.c_size_t)]
+               [("tile_rows", ctypes.c_int), ("max_tiles", ctypes.c_int), ("total", ctypes.c_size_t),
+                ("logits", ctypes.c_size_t)]
 
 
 class kmoe_stage_events(ctypes.Structure):
@@ -87,9 +89,13 @@ def load_library(path: str = LIB_PATH):
     lib.kmoe_mma_peak_run.restype = ctypes.c_int
     lib.kmoe_forward_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, V]
     lib.kmoe_forward_noalloc.restype = ctypes.c_int
+    lib.kmoe_router_workspace_size.restype = S
+    lib.kmoe_router_workspace_size.argtypes = [I]
+    lib.kmoe_router.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, V]
+    lib.kmoe_forward_router.argtypes = [pp, P, P, P, P, P, P, P, S, V, ctypes.POINTER(kmoe_stage_events)]
     for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
               "kmoe_prepare_weights", "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error",
-              "kmoe_selftest_wait_timeout"):
+              "kmoe_selftest_wait_timeout", "kmoe_router", "kmoe_forward_router"):
         getattr(lib, n).restype = ctypes.c_int
     return lib
 
@@ -227,6 +233,56 @@ def kmoe_forward(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=None, ou
     return out, workspace
 
 
+def kmoe_router_workspace_size(T: int) -> int:
+    return _lib.kmoe_router_workspace_size(T)
+
+
+def kmoe_router(x, w_gate, bias, k, logits=None, topk_ids=None, topk_w=None, workspace=None, stream=None):
+    """The fused router: logits = x @ w_gate^T (bf16 operands, fp32) and the
+    top-k routing of kmoe_route, in one kernel.  Returns (topk_ids, topk_w,
+    logits, workspace); the workspace's first word is the device error word."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(w_gate, "w_gate", torch.bfloat16)
+    _dev(bias, "bias", torch.float32)
+    T, H = x.shape
+    E = w_gate.shape[0]
+    if w_gate.shape[1] != H:
+        raise ValueError(f"w_gate must be [E, {H}], got {tuple(w_gate.shape)}")
+    dev = x.device
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(kmoe_router_workspace_size(T), dtype=torch.uint8, device=dev)
+    _check("kmoe_router", _lib.kmoe_router(_ptr(x), _ptr(w_gate), _ptr(bias), T, H, E, k, _ptr(logits),
+                                           _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), workspace.numel(),
+                                           _stream(stream)))
+    return topk_ids, topk_w, logits, workspace
+
+
+def kmoe_forward_router(p, x, w_gate, bias, w13_k, w2_k, out=None, workspace=None, stream=None,
+                        stage_events=None):
+    """kmoe_forward with the fused router (routing from x and the gate weight
+    instead of given logits).  stage_events: optional list of 7 torch.cuda.Event."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(w_gate, "w_gate", torch.bfloat16)
+    _dev(bias, "bias", torch.float32)
+    _dev(w13_k, "w13_k", torch.uint8)
+    _dev(w2_k, "w2_k", torch.uint8)
+    if out is None:
+        out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(kmoe_workspace_size(p), dtype=torch.uint8, device=x.device)
+    ev = None if stage_events is None else kmoe_stage_events(*[e.cuda_event for e in stage_events])
+    _check("kmoe_forward_router", _lib.kmoe_forward_router(
+        ctypes.byref(p), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(w13_k), _ptr(w2_k), _ptr(out), _ptr(workspace),
+        workspace.numel(), _stream(stream), None if ev is None else ctypes.byref(ev)))
+    return out, workspace
+
+
 def kmoe_forward_noalloc(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=None, out=None,
                          device_error=None, stream=None):
     """kmoe_forward without a workspace argument, for hosts that cannot
@@ -287,4 +343,5 @@ def stage_views(p, workspace):
         "xsf": workspace[L.xsf:L.xsf + (p.H // 128) * L.max_tiles * ((L.tile_rows + 127) // 128) * 512],
         "isf": workspace[L.isf:L.isf + (p.I // 128) * L.max_tiles * ((L.tile_rows + 127) // 128) * 512],
         "y": v(L.y, R * p.H, torch.float32).view(R, p.H),
+        "logits": v(L.logits, p.T * p.E, torch.float32).view(p.T, p.E),
     }

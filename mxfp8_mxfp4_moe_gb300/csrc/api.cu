@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "router.cuh"
 
 namespace kmoe {
 cudaError_t launch_route(const float*, const float*, int, int, int, int32_t*, float*, cudaStream_t);
@@ -114,6 +115,41 @@ int num_sms() {
   return n;
 }
 
+// Tensor maps and launch of the fused router (router.cu) over caller memory.
+int run_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, int T, int H, int E, int k,
+               float* logits, int32_t* ids, float* wts, int* sync, uint32_t* err, cudaStream_t stream) {
+  RouterArgs a{};
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.k = k;
+  a.plan = plan_router(T, E);
+  a.bias = bias;
+  a.logits = logits;
+  a.ids = ids;
+  a.wts = wts;
+  a.sync = sync;
+  a.err = err;
+  a.budget_ns = kWaitBudgetNs;
+  RouterMaps m;
+  if (!make_map(&m.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_bf16, H, T, static_cast<uint64_t>(H) * 2, 64, 128) ||
+      !make_map(&m.g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_gate_bf16, H, E, static_cast<uint64_t>(H) * 2, 64,
+                static_cast<uint32_t>(a.plan.EN)))
+    return KMOE_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return KMOE_ERR_CUDA;
+  return launch_router(m, a, sms, stream) == cudaSuccess ? KMOE_OK : KMOE_ERR_CUDA;
+}
+
+// Shape and pointer checks of the fused router's inputs.
+int check_router_args(const void* x_bf16, const void* w_gate_bf16, const float* bias, int T, int H, int E, int k) {
+  if (T < 0 || H <= 0 || E <= 0 || E > kMaxE || k <= 0 || k > E || k > kMaxK) return KMOE_ERR_ARG;
+  if (H % 64 != 0 || E % 4 != 0) return KMOE_ERR_SHAPE;
+  if (T > 0 && (!x_bf16 || !w_gate_bf16 || !bias)) return KMOE_ERR_ARG;
+  if (T > 0 && (!aligned(x_bf16, 16) || !aligned(w_gate_bf16, 16))) return KMOE_ERR_ALIGN;
+  return KMOE_OK;
+}
+
 #define KMOE_CK(call)                           \
   do {                                          \
     if ((call) != cudaSuccess) return KMOE_ERR_CUDA; \
@@ -182,6 +218,7 @@ int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out) {
   out->tile_rows = L.BN;
   out->max_tiles = L.max_tiles;
   out->total = L.total;
+  out->logits = L.logits;
   return KMOE_OK;
 }
 
@@ -233,21 +270,27 @@ int kmoe_forward(const kmoe_params* p, const void* x_bf16, const float* logits, 
                          stream, nullptr);
 }
 
-int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
-                    const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
-                    void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream,
-                    const kmoe_stage_events* ev) {
+// The forward; routing from given ids/weights, from logits, or (w_gate set)
+// by the fused router from x and the gate weight.
+static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* logits, const void* w_gate,
+                        const float* bias, const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids,
+                        const float* topk_w, void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                        const kmoe_stage_events* ev) {
   int st = check_params(p);
   if (st != KMOE_OK) return st;
   Layout L;
   if (!make_layout(*p, L)) return KMOE_ERR_ARG;
+  if (w_gate) {
+    st = check_router_args(x_bf16, w_gate, bias, p->T, p->H, p->E, p->k);
+    if (st != KMOE_OK) return st;
+  }
   if (!workspace || ws_bytes < L.total) return KMOE_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KMOE_ERR_ALIGN;
   if (p->T == 0) return KMOE_OK;
   const bool given = topk_ids != nullptr;
   if ((topk_ids == nullptr) != (topk_w == nullptr)) return KMOE_ERR_ARG;
   if (!x_bf16 || !w13_k || !w2_k || !out_bf16) return KMOE_ERR_ARG;
-  if (!given && (!logits || !bias)) return KMOE_ERR_ARG;
+  if (!given && !w_gate && (!logits || !bias)) return KMOE_ERR_ARG;
   if (!aligned(x_bf16, 16) || !aligned(out_bf16, 16) || !aligned(w13_k, 256) || !aligned(w2_k, 256))
     return KMOE_ERR_ALIGN;
 
@@ -301,6 +344,10 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   if (given) {
     KMOE_CK(cudaMemcpyAsync(ids, topk_ids, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
     KMOE_CK(cudaMemcpyAsync(wts, topk_w, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
+  } else if (w_gate) {
+    st = run_router(x_bf16, w_gate, bias, T, H, E, k, reinterpret_cast<float*>(ws + L.logits), ids, wts,
+                    reinterpret_cast<int*>(ws + L.router_sync), err, stream);
+    if (st != KMOE_OK) return st;
   } else {
     KMOE_CK(launch_route(logits, bias, T, E, k, ids, wts, stream));
   }
@@ -328,6 +375,44 @@ int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logit
   KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));
   KMOE_CK(mark(ev ? ev->combined : nullptr));
   return KMOE_OK;
+}
+
+int kmoe_forward_ex(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
+                    const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
+                    void* out_bf16, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                    const kmoe_stage_events* ev) {
+  return forward_impl(p, x_bf16, logits, nullptr, bias, w13_k, w2_k, topk_ids, topk_w, out_bf16, workspace, ws_bytes,
+                      stream, ev);
+}
+
+int kmoe_forward_router(const kmoe_params* p, const void* x_bf16, const void* w_gate_bf16, const float* bias,
+                        const uint8_t* w13_k, const uint8_t* w2_k, void* out_bf16, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream, const kmoe_stage_events* ev) {
+  if (!w_gate_bf16) return KMOE_ERR_ARG;
+  return forward_impl(p, x_bf16, nullptr, w_gate_bf16, bias, w13_k, w2_k, nullptr, nullptr, out_bf16, workspace,
+                      ws_bytes, stream, ev);
+}
+
+size_t kmoe_router_workspace_size(int T) {
+  if (T < 0) return 0;
+  return 256 + align_up(static_cast<size_t>(2 + (T + 127) / 128) * 4, 256);
+}
+
+int kmoe_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, int T, int H, int E, int k,
+                float* logits, int32_t* topk_ids, float* topk_w, void* workspace, size_t ws_bytes,
+                cudaStream_t stream) {
+  int st = check_router_args(x_bf16, w_gate_bf16, bias, T, H, E, k);
+  if (st != KMOE_OK) return st;
+  if (!workspace || ws_bytes < kmoe_router_workspace_size(T)) return KMOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KMOE_ERR_ALIGN;
+  if (T == 0) return KMOE_OK;
+  if (!logits || !topk_ids || !topk_w) return KMOE_ERR_ARG;
+  if (!aligned(logits, 16)) return KMOE_ERR_ALIGN;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  KMOE_CK(cudaMemsetAsync(err, 0, 16, stream));
+  return run_router(x_bf16, w_gate_bf16, bias, T, H, E, k, logits, topk_ids, topk_w, reinterpret_cast<int*>(ws + 256),
+                    err, stream);
 }
 
 int kmoe_device_error(void* workspace, uint32_t* word, cudaStream_t stream) {

@@ -31,7 +31,7 @@ __host__ __device__ __forceinline__ size_t tile_sf_offset(int tile, int local_ro
 // ---------------------------------------------------------------- workspace
 struct Layout {
   size_t err, topk_ids, topk_w, counts, seg_start, tile_start, chunk_prefix, rank, row_of_slot, slot_of_row;
-  size_t xq, xsf, iq, isf, y, total;
+  size_t xq, xsf, iq, isf, y, logits, router_sync, total;
   int R, BN, nch, max_tiles, nchunk;
 };
 
@@ -76,6 +76,9 @@ __host__ inline bool make_layout(const kmoe_params& p, Layout& L) {
   L.iq = take(R * p.I);
   L.isf = take(static_cast<size_t>(p.I / 128) * L.max_tiles * L.nch * 512);
   L.y = take(R * p.H * 4);
+  // the fused router's outputs and counters (token counter, one per 128-token tile)
+  L.logits = take(static_cast<size_t>(p.T) * p.E * 4);
+  L.router_sync = take(static_cast<size_t>(2 + (p.T + 127) / 128) * 4);
   L.total = off;
   return true;
 }

@@ -1,0 +1,317 @@
+// The fused router: the gate GEMM (logits = x W_g^T, bf16 operands, fp32
+// accumulation) and the sigmoid + correction-bias top-k of every token in one
+// kernel (Kimi-K3 SM120 FlashInfer MXFP4 page, "Phase 1: serving call chain":
+// the TopK step consumes the gate's logits).
+//
+// One persistent CTA per SM, all co-resident (cooperative launch).
+//   warp 0        TMA producer: per K step of 64, the 128-token x tile and the
+//                 EN-expert gate tile (both bf16, 128-byte swizzle)
+//   warp 1        TMEM owner and MMA issuer: tcgen05.mma .kind::f16 (bf16 x
+//                 bf16 -> fp32), M = 128 tokens, N = EN experts, K = 16 per
+//                 instruction; two 256-column accumulators so that the
+//                 epilogue of one item overlaps the next item's main loop
+//   warps 2..5    epilogue: TMEM -> registers -> a swizzled smem tile ->
+//                 coalesced fp32 rows of the logits; then the item's token
+//                 tile completion counter is bumped (fence + atomic)
+//   warps 6..17   routing: take tokens one at a time from a global counter,
+//                 wait (bounded) until every expert chunk of the token's tile
+//                 is written, route the token (route_dev.cuh)
+// The GEMM warps join the routing pool when their work runs out, so routing
+// of finished token tiles overlaps the gate GEMM of the rest.  Every wait is
+// bounded; a wait that gives up sets the timeout bit and the token is left
+// masked (ids -1).
+#include "gemm_dev.cuh"  // named_barrier_and
+#include "route_dev.cuh"
+#include "router.cuh"
+
+namespace kmoe {
+namespace {
+
+constexpr int kWarps = 18;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kFirstRouteWarp = 6;
+constexpr int kStages = 3;
+constexpr int kATile = 128 * 128;           // 128 tokens x 64 bf16
+constexpr int kStage = kATile + 256 * 128;  // + up to 256 experts x 64 bf16
+constexpr int kStgOff = kStages * kStage;   // epilogue staging: 32 x 32 fp32 per warp
+constexpr int kBarOff = kStgOff + 4 * 4096;
+constexpr int kBiasOff = kBarOff + 256;
+constexpr int kIdxOff = kBiasOff + 4 * kMaxE;
+constexpr int kSmem = 1024 + kIdxOff + kWarps * 32 * 4;
+constexpr uint32_t kTmemCols = 512;  // two accumulators of up to 256 columns
+static_assert(kSmem <= 232448, "shared memory budget");
+
+// bf16 instruction descriptor of tcgen05.mma .kind::f16: fp32 D (bits 4-5 =
+// 1), A and B bf16 (bits 7-9, 10-12 = 1), both K-major, N>>3 at bit 17, M>>4
+// at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A x B^T over K = 16 (32 bytes of each smem row).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Routing warps: tokens are handed out in increasing order, so the first
+// tiles' tokens are routed while later tiles are still in the GEMM.
+template <int KPL>
+__device__ void route_pool(const RouterArgs& a, const float* s_b, int* s_idx, int lane) {
+  int* next = a.sync;
+  const int* tile_done = a.sync + 2;
+  const int need = a.plan.nch;
+  for (;;) {
+    int t = 0;
+    if (lane == 0) t = atomicAdd(next, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t >= a.T) break;
+    const int* c = tile_done + (t >> 7);
+    int ready = 1;
+    if (lane == 0 && ld_acquire_gpu(c) < need) {
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        __nanosleep(256);
+        if (ld_acquire_gpu(c) >= need) break;
+        if ((*reinterpret_cast<volatile uint32_t*>(a.err) & KMOE_DEVERR_TIMEOUT) ||
+            globaltimer_ns() - t0 > a.budget_ns) {
+          atomicOr(a.err, KMOE_DEVERR_TIMEOUT);
+          ready = 0;
+          break;
+        }
+      }
+    }
+    ready = __shfl_sync(0xffffffffu, ready, 0);
+    int32_t* ids_row = a.ids + static_cast<size_t>(t) * a.k;
+    float* w_row = a.wts + static_cast<size_t>(t) * a.k;
+    if (!ready) {
+      if (lane < a.k) {
+        ids_row[lane] = -1;
+        w_row[lane] = 0.f;
+      }
+      continue;
+    }
+    (void)ld_acquire_gpu(c);  // each lane's own acquire before it reads the logits
+    route_token<KPL>(a.logits + static_cast<size_t>(t) * a.E, s_b, a.E, a.k, lane, ids_row, w_row, s_idx);
+  }
+}
+
+template <int KPL>
+__global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_constant__ RouterMaps maps,
+                                                             const RouterArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_b = reinterpret_cast<float*>(smem + kBiasOff);
+  int* s_idx = reinterpret_cast<int*>(smem + kIdxOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < a.E; e += kThreads) s_b[e] = a.bias[e];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.x);
+    prefetch_tmap(&maps.g);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int EN = a.plan.EN, nch = a.plan.nch, items = a.plan.items;
+  const int KS = a.H / 64;
+  const uint64_t budget = a.budget_ns;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint32_t tx = kATile + static_cast<uint32_t>(EN) * 128;
+      const uint64_t pol_x = policy_evict_normal();
+      const uint64_t pol_g = policy_evict_last();  // the gate weight is re-read by every token tile
+      uint32_t n = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const int mt = it / nch, nc = it - mt * nch;
+        for (int ks = 0; ks < KS; ++ks, ++n) {
+          const int s = static_cast<int>(n % kStages);
+          const uint32_t ph = (n / kStages) & 1u;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * kStage;
+          mbar_arrive_expect_tx(&full[s], tx);
+          tma_load_2d(st, &maps.x, &full[s], 64 * ks, 128 * mt, pol_x);
+          tma_load_2d(st + kATile, &maps.g, &full[s], 64 * ks, EN * nc, pol_g);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA can exit
+        const uint32_t first = n > static_cast<uint32_t>(kStages) ? n - kStages : 0u;
+        for (uint32_t i = first; i < n; ++i)
+          mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1u, 20000000ull, nullptr, nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, static_cast<uint32_t>(EN));
+      const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
+      const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + kATile));
+      int s = 0;
+      uint32_t ph = 0, li = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++li) {
+        const uint32_t acc = li & 1u;
+        const uint32_t aph = (li >> 1) & 1u;
+        if (!mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * 256u;
+        for (int ks = 0; ks < KS; ++ks) {
+          if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = static_cast<uint64_t>(s) * (kStage >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(d, adesc0 + so + 2 * kk, bdesc0 + so + 2 * kk, idesc, (ks | kk) != 0);
+          tc_commit(&empty[s]);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+      }
+      tc_commit(done);
+      mbar_wait_bounded(done, 0, budget, a.err, nullptr);
+    }
+    __syncwarp();
+  } else if (warp < kFirstRouteWarp) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    float* stg = reinterpret_cast<float*>(smem + kStgOff) + (warp - 2) * 1024;
+    uint32_t li = 0;
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++li) {
+      const uint32_t acc = li & 1u;
+      const uint32_t aph = (li >> 1) & 1u;
+      bool ok = mbar_wait_bounded(&acc_full[acc], aph, budget, a.err, abort_flag);
+      ok = named_barrier_and(1, 128, ok && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int mt = it / nch, nc = it - mt * nch;
+      const int t0 = 128 * mt + 32 * q;
+      for (int c0 = 0; c0 < EN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * 256u + c0, r);
+        tmem_ld_wait();
+        // row `lane` of the 32 x 32 tile; its 16-byte unit u goes to u ^ (lane & 7)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) << 2)) =
+              make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]), __uint_as_float(r[4 * u + 2]),
+                          __uint_as_float(r[4 * u + 3]));
+        __syncwarp();
+        // 8 lanes per token row (128 contiguous bytes), 4 rows per store
+        const int e0 = nc * EN + c0 + 4 * (lane & 7);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3);
+          const int t = t0 + rr;
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + (((lane & 7) ^ (rr & 7)) << 2));
+          if (t < a.T && e0 < a.E) *reinterpret_cast<float4*>(a.logits + static_cast<size_t>(t) * a.E + e0) = v;
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      // publish: every writer's stores before the tile's counter moves
+      __threadfence();
+      named_barrier(1, 128);
+      if (warp == 2 && lane == 0) atomicAdd(a.sync + 2 + mt, 1);
+    }
+  }
+  route_pool<KPL>(a, s_b, s_idx + warp * 32, lane);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int KPL>
+cudaError_t launch_kpl(const RouterMaps& maps, const RouterArgs& a, int sms, cudaStream_t st) {
+  static int ready = 0;  // attribute set and occupancy checked (per instantiation; idempotent)
+  if (!ready) {
+    cudaError_t e = cudaFuncSetAttribute(router_kernel<KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, router_kernel<KPL>, kThreads, kSmem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    ready = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;  // the routing warps wait on other CTAs' tiles
+  at[0].val.cooperative = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(sms), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, router_kernel<KPL>, maps, a);
+}
+
+}  // namespace
+
+cudaError_t launch_router(const RouterMaps& maps, const RouterArgs& a, int sms, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  if (a.E % 4 != 0 || a.H % 64 != 0 || a.E > kMaxE || sms <= 0) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(a.sync, 0, router_sync_bytes(a.T), st);
+  if (e != cudaSuccess) return e;
+  if (a.E <= 64) return launch_kpl<2>(maps, a, sms, st);
+  if (a.E <= 256) return launch_kpl<8>(maps, a, sms, st);
+  return launch_kpl<32>(maps, a, sms, st);
+}
+
+}  // namespace kmoe

@@ -65,6 +65,20 @@ def test_host_side_argument_errors(K):
         st = lib.kmoe_forward(ctypes.byref(p), None, None, None, None, None, None, None, None, None, 0, None)
         assert st in (1, 2)
     assert lib.kmoe_route(None, None, 4, 8, 9, None, None, None) == 1
+    # the fused router: shapes, pointers, alignment and workspace are checked on the host
+    nr = K.kmoe_router_workspace_size(300)
+    assert nr == 256 + 256 and K.kmoe_router_workspace_size(-1) == 0
+    r = lib.kmoe_router
+    assert r(16, 16, 16, 4, 128, 6, 2, 16, 16, 16, 256, nr, None) == 2      # E not a multiple of 4
+    assert r(16, 16, 16, 4, 96, 8, 2, 16, 16, 16, 256, nr, None) == 2       # H not a multiple of 64
+    assert r(16, 16, 16, 4, 128, 8, 9, 16, 16, 16, 256, nr, None) == 1      # k > E
+    assert r(None, 16, 16, 4, 128, 8, 2, 16, 16, 16, 256, nr, None) == 1    # no x
+    assert r(8, 16, 16, 4, 128, 8, 2, 16, 16, 16, 256, nr, None) == 3       # x not 16-byte aligned
+    assert r(16, 16, 16, 4, 128, 8, 2, 16, 16, 16, 256, 16, None) == 5      # workspace too small
+    assert r(16, 16, 16, 4, 128, 8, 2, 16, 16, 16, 128, nr, None) == 3      # workspace not 256-byte aligned
+    assert r(16, 16, 16, 4, 128, 8, 2, 8, 16, 16, 256, nr, None) == 3       # logits not 16-byte aligned
+    pr = K.make_params(16, 128, 128, 6, 2)
+    assert lib.kmoe_forward_router(ctypes.byref(pr), 16, 16, 16, 256, 256, 16, 256, 1 << 30, None, None) == 2
     assert lib.kmoe_quantize_mx(None, 4, 100, 0, None, None, None) == 2
     assert lib.kmoe_quantize_mx(None, 4, 128, 7, None, None, None) == 1
     p = K.make_params(16, 128, 128, 8, 2)
