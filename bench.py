@@ -197,6 +197,8 @@ class Layer:
         s = W.gen_small_inputs(w)
         self.host = s
         self.x = torch.from_numpy(s["x"].view(np.int16)).view(torch.bfloat16).to(device)
+        self.wg = torch.from_numpy(s["wg"].view(np.int16)).view(torch.bfloat16).to(device)
+        self.router = False  # True: route from x and the gate weight (kmoe_forward_router)
         self.logits = torch.from_numpy(s["logits"]).to(device)
         self.bias = torch.from_numpy(s["bias"]).to(device)
         self.p = layer_params(K, w)
@@ -216,6 +218,11 @@ class Layer:
 
     def forward(self, stage_events=False, x=None, logits=None, bias=None, out=None):
         wt = self.weights
+        if self.router:
+            self.K.kmoe_forward_router(self.p, self.x if x is None else x, self.wg, self.bias if bias is None else bias,
+                                       wt["w13_k"], wt["w2_k"], out=self.out if out is None else out,
+                                       workspace=self.ws, stage_events=self.events if stage_events else None)
+            return
         self.K.kmoe_forward(self.p, self.x if x is None else x, self.logits if logits is None else logits,
                             self.bias if bias is None else bias, wt["w13_k"], wt["w2_k"],
                             out=self.out if out is None else out, workspace=self.ws,
@@ -295,6 +302,50 @@ def mma_peak(device, N=224, iters=500000):
     return {"tflops": flops / (ms / 1e3) / 1e12, "N": N, "duration_ms": ms,
             "what": "tcgen05.mma kind::mxf8f6f4 block-scaled E2M1 x E4M3, M=128, operands resident in smem, "
                     "one CTA per SM"}
+
+
+def time_router(w, device, iters=20):
+    """The fused router (kmoe_router) alone on workload w, with the L2 flushed
+    (a 256 MB write) before every timed launch; beside it, for context, the
+    routing kernel alone on the same logits (kmoe_route) and a cuBLAS bf16
+    GEMM of the same shape (torch.matmul, bf16 output)."""
+    import torch
+    import mxfp8_mxfp4_moe_gb300 as K
+    s = W.gen_small_inputs(w)
+    x = torch.from_numpy(s["x"].view(np.int16)).view(torch.bfloat16).to(device)
+    wg = torch.from_numpy(s["wg"].view(np.int16)).view(torch.bfloat16).to(device)
+    bias = torch.from_numpy(s["bias"]).to(device)
+    logits = torch.empty((w.T, w.E), dtype=torch.float32, device=device)
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=device)
+    wts = torch.empty((w.T, w.k), dtype=torch.float32, device=device)
+    ws = torch.zeros(K.kmoe_router_workspace_size(w.T, w.H, w.E), dtype=torch.uint8, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for _ in range(iters):
+            flush.zero_()
+            ev[0].record()
+            fn()
+            ev[1].record()
+            torch.cuda.synchronize()
+            tot += ev[0].elapsed_time(ev[1])
+        return tot / iters
+
+    t_router = timed(lambda: K.kmoe_router(x, wg, bias, w.k, logits, ids, wts, ws))
+    st, word = K.kmoe_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"router device error {word:#x}")
+    t_route = timed(lambda: K.kmoe_route(logits, bias, w.k, ids, wts))
+    t_cublas = timed(lambda: torch.matmul(x, wg.t()))
+    flops = 2.0 * w.T * w.H * w.E
+    nbytes = 2.0 * w.T * w.H + 2.0 * w.E * w.H + 4.0 * w.T * w.E + 8.0 * w.T * w.k + 4.0 * w.E
+    return {"router_ms": t_router, "route_kernel_only_ms": t_route, "cublas_bf16_gemm_ms": t_cublas,
+            "gemm_tflops": flops / (t_router / 1e3) / 1e12, "algorithmic_GBs": nbytes / (t_router / 1e3) / 1e9,
+            "flop": flops, "algorithmic_bytes": nbytes}
 
 
 def e2e_time(layer, steps, warmup):
@@ -476,8 +527,33 @@ def run_ours(args):
         "tflops": wsg.flops() / (sg_ms / 1e3) / 1e12,
         "stages_ms": dict(zip(K.STAGE_NAMES, sg_stages)),
     }
-    del sl, weights
+    # ---- the fused router (gate GEMM + routing in one kernel) on the same prefill layer
+    rl_ = Layer(wp, device, weights=weights)
+    rl_.router = True
+    fr_total, _ = time_layer(rl_, args.steps, args.warmup, dist, device, None)
+    fr_total = reduce_max(dist, fr_total, device)
+    fr_ms = fr_total / args.steps
+    fr_stages = time_stages(rl_, max(3, min(args.steps, 10)))
+    rl_.check()
+    del sl, rl_, weights
     torch.cuda.empty_cache()
+    r_pre = time_router(wp, device)
+    r_dec = time_router(W.WORKLOADS[DECODE], device)
+    router = {
+        "what": "gate GEMM (bf16 x bf16 -> fp32 logits on tcgen05) and sigmoid + bias top-16 routing in one "
+                "kernel; L2 flushed before each timed launch",
+        "prefill_T8192": r_pre, "decode_T16": r_dec,
+        "layer_with_fused_router_T8192": {"ms_per_layer": fr_ms, "tokens_per_s": wp.T / (fr_ms / 1e3),
+                                          "stages_ms": dict(zip(K.STAGE_NAMES, fr_stages))},
+        "roofline": {"bound": "tensor", "kernel": "router_kernel (prefill T=8192)",
+                     "achieved": r_pre["gemm_tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": r_pre["gemm_tflops"] / peaks["bf16_tflops"],
+                     "peak_source": f"{peaks_kind}: bf16_tflops (burst; the kernel is timed alone)",
+                     "algorithmic": "2*T*H*E FLOP per launch"},
+        "decode_roofline": {"bound": "hbm", "achieved": r_dec["algorithmic_GBs"], "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": r_dec["algorithmic_GBs"] / peaks["hbm_gbs"],
+                            "algorithmic": "x + gate weight + bias read, logits/ids/weights written"},
+    }
 
     # ---- the real checkpoint's expert shape (3584-wide latent, I=3072): prefill and decode
     wr = W.NEXT_WORKLOADS["real_prefill"]
@@ -543,6 +619,7 @@ def run_ours(args):
             "mma_peak_measured": peak_mma,
             "real_shape": real_shape,
             "swiglu_control": swiglu_control,
+            "router": router,
             "decode": {"workload": "Kimi-K3 MoE layer decode T=16 H=7168 I=3584 E=896 top-16",
                        "us_per_layer": d_us, "touched_experts": touched, "layer_GBs": d_layer_gbs,
                        "layer_hbm_frac": d_layer_gbs / peaks["hbm_gbs"],
@@ -567,8 +644,9 @@ def run_ours(args):
 def run_profile(args):
     """Lean mode for profiler captures: one workload, warm-up + steps forwards,
     stage times printed as JSON (no clocks, baselines or e2e).  "route:NAME"
-    runs only the routing kernel on workload NAME's logits (no weights on the
-    device), for multi-pass captures of that kernel."""
+    runs only the routing kernel on workload NAME's logits and "router:NAME"
+    only the fused router on its x and gate weight (no expert weights on the
+    device), for multi-pass captures of those kernels."""
     import torch
     torch.cuda.set_device(0)
     if args.profile.startswith("route:"):
@@ -584,6 +662,20 @@ def run_profile(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": args.profile, "T": w.T, "E": w.E, "k": w.k}))
         return 0
+    if args.profile.startswith("router:"):
+        import mxfp8_mxfp4_moe_gb300 as K
+        w = W.WORKLOADS[args.profile.split(":", 1)[1]]
+        s = W.gen_small_inputs(w)
+        x = torch.from_numpy(s["x"].view(np.int16)).view(torch.bfloat16).cuda()
+        wg = torch.from_numpy(s["wg"].view(np.int16)).view(torch.bfloat16).cuda()
+        bias = torch.from_numpy(s["bias"]).cuda()
+        ws = torch.zeros(K.kmoe_router_workspace_size(w.T, w.H, w.E), dtype=torch.uint8, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            K.kmoe_router(x, wg, bias, w.k, workspace=ws)
+        torch.cuda.synchronize()
+        st, word = K.kmoe_device_error(ws)
+        print(json.dumps({"profile": args.profile, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "device_error": word}))
+        return 0 if st == 0 else 1
     w = {**W.WORKLOADS, **W.PROFILE_WORKLOADS}[args.profile]
     layer = Layer(w, torch.device("cuda", 0))
     for _ in range(args.warmup + args.steps):

@@ -139,22 +139,24 @@ int kmoe_route(const float* logits, const float* bias, int T, int E, int k, int3
 /* The router (Kimi-K3 SM120 FlashInfer MXFP4 page, "Phase 1: serving call
  * chain": TopK consumes the gate's logits), fused: the gate GEMM
  *   logits[t, e] = sum_h x[t, h] * w_gate[e, h]
- * on the tensor cores (bf16 x bf16, fp32 accumulation, a fixed summation
- * order for a given (T, H, E)), followed in the same kernel by the routing of
+ * on the tensor cores (bf16 x bf16, fp32 accumulation; the summation order,
+ * split K included, depends only on (T, H, E)), followed in the same kernel by the routing of
  * kmoe_route on those logits; tokens of finished 128-token tiles are routed
  * while the gate GEMM of later tiles runs.
  *   x [T, H] bf16 and w_gate [E, H] bf16 (both row-major, 16-byte aligned),
  *   bias [E] float; logits [T, E] float (out, 16-byte aligned), topk_ids
  *   [T, k] int32 (out), topk_w [T, k] float (out).  H a multiple of 64, E a
  *   multiple of 4 and <= 1024, k <= min(E, 32).
- *   workspace: device memory of kmoe_router_workspace_size(T) bytes, 256-byte
- *   aligned, caller-owned; its first word is the device error word (read it
- *   with kmoe_device_error).  The call launches one CTA per SM as a
+ *   workspace: device memory of kmoe_router_workspace_size(T, H, E) bytes
+ *   (0 for invalid sizes), 256-byte aligned, caller-owned: counters and, when
+ *   few token tiles leave SMs idle (decode), the partial sums of a split K;
+ *   its first word is the device error word (read it with
+ *   kmoe_device_error).  The call launches one CTA per SM as a
  *   cooperative launch (all co-resident), so it fails with KMOE_ERR_CUDA if
  *   the device cannot host them all at once.  Every device wait is bounded;
  *   a token whose logits did not arrive in time is left masked (ids -1,
  *   weights 0) and the timeout bit is set. */
-size_t kmoe_router_workspace_size(int T);
+size_t kmoe_router_workspace_size(int T, int H, int E);
 int kmoe_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, int T, int H, int E, int k,
                 float* logits, int32_t* topk_ids, float* topk_w, void* workspace, size_t ws_bytes,
                 cudaStream_t stream);

@@ -90,7 +90,7 @@ def load_library(path: str = LIB_PATH):
     lib.kmoe_forward_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, V]
     lib.kmoe_forward_noalloc.restype = ctypes.c_int
     lib.kmoe_router_workspace_size.restype = S
-    lib.kmoe_router_workspace_size.argtypes = [I]
+    lib.kmoe_router_workspace_size.argtypes = [I, I, I]
     lib.kmoe_router.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, V]
     lib.kmoe_forward_router.argtypes = [pp, P, P, P, P, P, P, P, S, V, ctypes.POINTER(kmoe_stage_events)]
     for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
@@ -233,8 +233,8 @@ def kmoe_forward(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=None, ou
     return out, workspace
 
 
-def kmoe_router_workspace_size(T: int) -> int:
-    return _lib.kmoe_router_workspace_size(T)
+def kmoe_router_workspace_size(T: int, H: int, E: int) -> int:
+    return _lib.kmoe_router_workspace_size(T, H, E)
 
 
 def kmoe_router(x, w_gate, bias, k, logits=None, topk_ids=None, topk_w=None, workspace=None, stream=None):
@@ -256,7 +256,7 @@ def kmoe_router(x, w_gate, bias, k, logits=None, topk_ids=None, topk_w=None, wor
     if topk_w is None:
         topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = torch.empty(kmoe_router_workspace_size(T), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(kmoe_router_workspace_size(T, H, E), dtype=torch.uint8, device=dev)
     _check("kmoe_router", _lib.kmoe_router(_ptr(x), _ptr(w_gate), _ptr(bias), T, H, E, k, _ptr(logits),
                                            _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), workspace.numel(),
                                            _stream(stream)))

@@ -117,22 +117,25 @@ int num_sms() {
 
 // Tensor maps and launch of the fused router (router.cu) over caller memory.
 int run_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, int T, int H, int E, int k,
-               float* logits, int32_t* ids, float* wts, int* sync, uint32_t* err, cudaStream_t stream) {
+               float* logits, float* part, int32_t* ids, float* wts, int* sync, uint32_t* err, cudaStream_t stream) {
   RouterArgs a{};
   a.T = T;
   a.H = H;
   a.E = E;
   a.k = k;
-  a.plan = plan_router(T, E);
+  a.xrows = T <= 32 ? 32 : (T <= 64 ? 64 : 128);
+  a.plan = plan_router(T, H, E);
   a.bias = bias;
   a.logits = logits;
+  a.part = part;
   a.ids = ids;
   a.wts = wts;
   a.sync = sync;
   a.err = err;
   a.budget_ns = kWaitBudgetNs;
   RouterMaps m;
-  if (!make_map(&m.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_bf16, H, T, static_cast<uint64_t>(H) * 2, 64, 128) ||
+  if (!make_map(&m.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_bf16, H, T, static_cast<uint64_t>(H) * 2, 64,
+                static_cast<uint32_t>(a.xrows)) ||
       !make_map(&m.g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_gate_bf16, H, E, static_cast<uint64_t>(H) * 2, 64,
                 static_cast<uint32_t>(a.plan.EN)))
     return KMOE_ERR_CUDA;
@@ -345,7 +348,8 @@ static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* l
     KMOE_CK(cudaMemcpyAsync(ids, topk_ids, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
     KMOE_CK(cudaMemcpyAsync(wts, topk_w, static_cast<size_t>(R) * 4, cudaMemcpyDeviceToDevice, stream));
   } else if (w_gate) {
-    st = run_router(x_bf16, w_gate, bias, T, H, E, k, reinterpret_cast<float*>(ws + L.logits), ids, wts,
+    st = run_router(x_bf16, w_gate, bias, T, H, E, k, reinterpret_cast<float*>(ws + L.logits),
+                    reinterpret_cast<float*>(ws + L.router_part), ids, wts,
                     reinterpret_cast<int*>(ws + L.router_sync), err, stream);
     if (st != KMOE_OK) return st;
   } else {
@@ -393,9 +397,10 @@ int kmoe_forward_router(const kmoe_params* p, const void* x_bf16, const void* w_
                       ws_bytes, stream, ev);
 }
 
-size_t kmoe_router_workspace_size(int T) {
-  if (T < 0) return 0;
-  return 256 + align_up(static_cast<size_t>(2 + (T + 127) / 128) * 4, 256);
+size_t kmoe_router_workspace_size(int T, int H, int E) {
+  if (T < 0 || H <= 0 || H % 64 != 0 || E <= 0 || E > kMaxE) return 0;
+  const RouterPlan rp = plan_router(T, H, E);
+  return 256 + align_up(router_sync_bytes(rp), 256) + align_up(router_part_bytes(rp, T, E), 256);
 }
 
 int kmoe_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, int T, int H, int E, int k,
@@ -403,7 +408,7 @@ int kmoe_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, 
                 cudaStream_t stream) {
   int st = check_router_args(x_bf16, w_gate_bf16, bias, T, H, E, k);
   if (st != KMOE_OK) return st;
-  if (!workspace || ws_bytes < kmoe_router_workspace_size(T)) return KMOE_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < kmoe_router_workspace_size(T, H, E)) return KMOE_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KMOE_ERR_ALIGN;
   if (T == 0) return KMOE_OK;
   if (!logits || !topk_ids || !topk_w) return KMOE_ERR_ARG;
@@ -411,8 +416,10 @@ int kmoe_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);
   KMOE_CK(cudaMemsetAsync(err, 0, 16, stream));
-  return run_router(x_bf16, w_gate_bf16, bias, T, H, E, k, logits, topk_ids, topk_w, reinterpret_cast<int*>(ws + 256),
-                    err, stream);
+  const RouterPlan rp = plan_router(T, H, E);
+  float* part = reinterpret_cast<float*>(ws + 256 + align_up(router_sync_bytes(rp), 256));
+  return run_router(x_bf16, w_gate_bf16, bias, T, H, E, k, logits, part, topk_ids, topk_w,
+                    reinterpret_cast<int*>(ws + 256), err, stream);
 }
 
 int kmoe_device_error(void* workspace, uint32_t* word, cudaStream_t stream) {

@@ -28,10 +28,68 @@ __host__ __device__ __forceinline__ size_t tile_sf_offset(int tile, int local_ro
   return ((static_cast<size_t>(tile) * KB + kb) * nch + chunk) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (g & 3);
 }
 
+// ---------------------------------------------------------------- fused router plan
+// Work decomposition of the gate GEMM (router.cu): token tiles of 128 rows
+// (the MMA's M) times expert chunks of EN columns (the MMA's N), optionally
+// times S splits of K (= H) when there are too few items to occupy the SMs;
+// the last split of a (tile, chunk) to finish sums the S partial tiles in
+// split order.  The plan depends on the shape only (never on the device), so
+// the logits' rounding is the same on every GPU.
+struct RouterPlan {
+  int EN;     // experts per item, a multiple of 32 in [32, 256]
+  int nch;    // expert chunks: ceil(E / EN)
+  int tiles;  // token tiles: ceil(T / 128)
+  int S;      // K splits
+  int kper;   // 64-wide K steps per split (the last split may have fewer)
+  int items;  // tiles * nch * S
+};
+
+// EN minimises (rounds of items over 152 SMs) x (MMA time per K step,
+// proportional to EN above ~112 columns, flat below); ties go to the smaller
+// EN (more SMs streaming the gate weight).  Fewer than 76 items: K is split
+// so that about 152 items run, each with at least 8 K steps.
+__host__ inline RouterPlan plan_router(int T, int H, int E) {
+  constexpr int kSlots = 152;
+  RouterPlan best{};
+  long long best_cost = -1;
+  const int tiles = (T + 127) / 128;
+  for (int en = 32; en <= 256; en += 32) {
+    const int nch = (E + en - 1) / en;
+    const long long items = static_cast<long long>(tiles) * nch;
+    const long long rounds = (items + kSlots - 1) / kSlots;
+    const long long cost = rounds * (en > 112 ? en : 112);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = RouterPlan{en, nch, tiles, 1, 0, static_cast<int>(items)};
+    }
+  }
+  const int KS = H / 64;
+  const int base = best.items;
+  int S = 1;
+  if (base > 0 && base < kSlots / 2) {
+    S = kSlots / base;
+    const int smax = KS / 8 > 1 ? KS / 8 : 1;
+    if (S > smax) S = smax;
+  }
+  best.kper = (KS + S - 1) / S;
+  best.S = (KS + best.kper - 1) / best.kper;  // no empty split
+  best.items = base * best.S;
+  return best;
+}
+
+// Router counters: the routing warps' token counter, one completion counter
+// per token tile, one split counter per (tile, chunk).
+__host__ inline size_t router_sync_bytes(const RouterPlan& r) {
+  return static_cast<size_t>(2 + r.tiles + r.tiles * r.nch) * 4;
+}
+__host__ inline size_t router_part_bytes(const RouterPlan& r, int T, int E) {
+  return r.S > 1 ? static_cast<size_t>(r.S) * T * E * 4 : 0;
+}
+
 // ---------------------------------------------------------------- workspace
 struct Layout {
   size_t err, topk_ids, topk_w, counts, seg_start, tile_start, chunk_prefix, rank, row_of_slot, slot_of_row;
-  size_t xq, xsf, iq, isf, y, logits, router_sync, total;
+  size_t xq, xsf, iq, isf, y, logits, router_sync, router_part, total;
   int R, BN, nch, max_tiles, nchunk;
 };
 
@@ -78,7 +136,9 @@ __host__ inline bool make_layout(const kmoe_params& p, Layout& L) {
   L.y = take(R * p.H * 4);
   // the fused router's outputs and counters (token counter, one per 128-token tile)
   L.logits = take(static_cast<size_t>(p.T) * p.E * 4);
-  L.router_sync = take(static_cast<size_t>(2 + (p.T + 127) / 128) * 4);
+  const RouterPlan rp = plan_router(p.T, p.H, p.E);
+  L.router_sync = take(router_sync_bytes(rp));
+  L.router_part = take(router_part_bytes(rp, p.T, p.E));
   L.total = off;
   return true;
 }

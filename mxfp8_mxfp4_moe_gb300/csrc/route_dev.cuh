@@ -5,13 +5,19 @@
 //
 // Lane l holds the keys of experts l, l+32, l+64, ...  The selection key is
 // fp32(sigmoid(logit)) + fp32(bias) with the sigmoid correctly rounded to fp32
-// (evaluated in double).  Double precision is slow on this part, so a radix
-// select first finds the k-th largest cheap fp32 key, and only experts whose
-// cheap key lies within a safety margin of it (the margin is far above the
-// error of expf) get the exact key; the final top-k is taken over exact keys,
-// equal keys going to the lower expert index.  Usually the candidates fit one
-// per lane and are ranked in one pass; with more than 32 (many equal keys) k
-// rounds of warp arg-max are used instead.
+// (evaluated in double).  Double precision is slow on this part, so the top-k
+// is first narrowed with cheap fp32 keys (expf; their error is far below the
+// safety margin used below) and only the candidates get the exact key; the
+// final top-k is taken over exact keys, equal keys going to the lower expert
+// index.
+//   1. A lower bound of the k-th largest cheap key: the k-th largest of the
+//      32 lane maxima (k lanes each hold a key at least that large).  Experts
+//      whose cheap key is within the margin of it are the candidates; usually
+//      they fit one per lane and are ranked by exact key in one pass.
+//   2. Otherwise (more than 32 candidates), the exact k-th largest cheap key
+//      by a bitwise radix select, and the candidates within the margin of it.
+//   3. If those are still more than 32 (many equal keys): k rounds of warp
+//      arg-max over the candidates' exact keys.
 //
 // Used by the routing kernel (logits given) and by the fused router kernel
 // (logits produced by its own GEMM phase).
@@ -54,6 +60,59 @@ __device__ __forceinline__ float exact_key(const float* lg, const float* bias, i
   return isnan(kx) ? -__int_as_float(0x7f800000) : kx;
 }
 
+// Cut (an order key) for the candidates of a k-th largest cheap key `kth`:
+// everything within the safety margin below it.
+__device__ __forceinline__ uint32_t candidate_cut(float kth) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
+  return order_key((kth == NEG_INF) ? NEG_INF : kth - margin);
+}
+
+// Candidates (order key >= ocut) one per lane, ranked by exact key across the
+// warp; writes the top k and returns true, or returns false (nothing written)
+// when there are more than 32 candidates.
+template <int KPL>
+__device__ __forceinline__ bool select_ranked(const uint32_t (&okey)[KPL], uint32_t ocut, const float* lg,
+                                              const float* bias, int E, int k, int lane, int32_t* ids_row,
+                                              float* wts_row, int* s_idx) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int e = lane + 32 * i;
+    const bool pred = e < E && okey[i] >= ocut;
+    const unsigned m = __ballot_sync(0xffffffffu, pred);
+    const int pos = base + __popc(m & ((1u << lane) - 1u));
+    if (pred && pos < 32) s_idx[pos] = e;
+    base += __popc(m);
+  }
+  __syncwarp();
+  if (base > 32) {
+    __syncwarp();
+    return false;
+  }
+  const bool have = lane < base;
+  const int idx = have ? s_idx[lane] : 0x7fffffff;
+  float sv = 0.f;
+  const float kx = have ? exact_key(lg, bias, idx, sv) : NEG_INF;
+  int rank = 0;
+  for (int j = 0; j < 32; ++j) {
+    const float kj = __shfl_sync(0xffffffffu, kx, j);
+    const int ij = __shfl_sync(0xffffffffu, idx, j);
+    rank += (kj > kx || (kj == kx && ij < idx)) ? 1 : 0;
+  }
+  const bool sel = have && rank < k;
+  double sum = sel ? static_cast<double>(sv) : 0.0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (sel) {
+    ids_row[rank] = idx;
+    wts_row[rank] = static_cast<float>(static_cast<double>(sv) / sum);
+  }
+  __syncwarp();  // s_idx is reused by this warp's next token
+  return true;
+}
+
 // Routes one token.  `lg` (the token's E logits) and `bias` may be in shared
 // or global memory (generic pointers; global data must already be visible to
 // this thread).  `s_idx` is 32 ints of this warp's shared memory.  Writes the
@@ -63,13 +122,14 @@ __device__ __forceinline__ void route_token(const float* lg, const float* bias, 
                                             int32_t* ids_row, float* wts_row, int* s_idx) {
   const float NEG_INF = -__int_as_float(0x7f800000);
   // only the integer images of the cheap keys live in registers
-  uint32_t okey[KPL];  // 0 for absent experts: below every probe
+  uint32_t okey[KPL];  // 0 for absent experts: below every key
   float lv[KPL];
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = lane + 32 * i;
     lv[i] = e < E ? lg[e] : 0.f;
   }
+  uint32_t lmax = 0;
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = lane + 32 * i;
@@ -78,9 +138,22 @@ __device__ __forceinline__ void route_token(const float* lg, const float* bias, 
       const float kf = 1.f / (1.f + expf(-lv[i])) + bias[e];
       okey[i] = order_key(isnan(kf) ? NEG_INF : kf);
     }
+    lmax = okey[i] > lmax ? okey[i] : lmax;
   }
-  // pass 1: the k-th largest cheap key, by a bitwise radix select over the
-  // integer images (32 counting rounds)
+  // 1. the k-th largest lane maximum (ranks 0..31, ties by lane) bounds the
+  //    k-th largest cheap key from below
+  {
+    int rank = 0;
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t o = __shfl_sync(0xffffffffu, lmax, j);
+      rank += (o > lmax || (o == lmax && j < lane)) ? 1 : 0;
+    }
+    const unsigned who = __ballot_sync(0xffffffffu, rank == k - 1);
+    const float lb = order_key_inverse(__shfl_sync(0xffffffffu, lmax, __ffs(who) - 1));
+    if (select_ranked<KPL>(okey, candidate_cut(lb), lg, bias, E, k, lane, ids_row, wts_row, s_idx)) return;
+  }
+  // 2. the exact k-th largest cheap key, by a bitwise radix select over the
+  //    integer images (32 counting rounds)
   uint32_t prefix = 0;
   for (int bit = 31; bit >= 0; --bit) {
     const uint32_t probe = prefix | (1u << bit);
@@ -89,50 +162,11 @@ __device__ __forceinline__ void route_token(const float* lg, const float* bias, 
     for (int i = 0; i < KPL; ++i) cnt += okey[i] >= probe;
     if (static_cast<int>(__reduce_add_sync(0xffffffffu, cnt)) >= k) prefix = probe;
   }
-  const float kth = order_key_inverse(prefix);
-  // candidates: cheap key within the margin of the k-th
-  const float margin = 1e-5f * fmaxf(1.f, fabsf(kth));
-  const uint32_t ocut = order_key((kth == NEG_INF) ? NEG_INF : kth - margin);
-
-  // fast path: the candidates one per lane, exact keys ranked across the warp
-  {
-    int base = 0;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      const int e = lane + 32 * i;
-      const bool pred = e < E && okey[i] >= ocut;
-      const unsigned m = __ballot_sync(0xffffffffu, pred);
-      const int pos = base + __popc(m & ((1u << lane) - 1u));
-      if (pred && pos < 32) s_idx[pos] = e;
-      base += __popc(m);
-    }
-    __syncwarp();
-    if (base <= 32) {
-      const bool have = lane < base;
-      const int idx = have ? s_idx[lane] : 0x7fffffff;
-      float sv = 0.f;
-      const float kx = have ? exact_key(lg, bias, idx, sv) : NEG_INF;
-      int rank = 0;
-      for (int j = 0; j < 32; ++j) {
-        const float kj = __shfl_sync(0xffffffffu, kx, j);
-        const int ij = __shfl_sync(0xffffffffu, idx, j);
-        rank += (kj > kx || (kj == kx && ij < idx)) ? 1 : 0;
-      }
-      const bool sel = have && rank < k;
-      double sum = sel ? static_cast<double>(sv) : 0.0;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (sel) {
-        ids_row[rank] = idx;
-        wts_row[rank] = static_cast<float>(static_cast<double>(sv) / sum);
-      }
-      __syncwarp();  // s_idx is reused by this warp's next token
-      return;
-    }
-  }
-  // general path (more than 32 candidates, e.g. many equal keys): k rounds of
-  // warp arg-max over the exact keys of the candidates not taken yet (exact
-  // keys recomputed each round: this path is rare)
+  const uint32_t ocut = candidate_cut(order_key_inverse(prefix));
+  if (select_ranked<KPL>(okey, ocut, lg, bias, E, k, lane, ids_row, wts_row, s_idx)) return;
+  // 3. more than 32 candidates (e.g. many equal keys): k rounds of warp
+  //    arg-max over the exact keys of the candidates not taken yet (exact keys
+  //    recomputed each round: this path is rare)
   uint32_t taken = 0;
   float mys = 0.f;
   int myid = -1;

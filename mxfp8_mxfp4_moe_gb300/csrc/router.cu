@@ -4,16 +4,22 @@
 // the TopK step consumes the gate's logits).
 //
 // One persistent CTA per SM, all co-resident (cooperative launch).
-//   warp 0        TMA producer: per K step of 64, the 128-token x tile and the
-//                 EN-expert gate tile (both bf16, 128-byte swizzle)
+//   warp 0        TMA producer: per K step of 64, the x tile (128 tokens, or
+//                 32 / 64 when T is that small) and the EN-expert gate tile
+//                 (both bf16, 128-byte swizzle); as many pipeline stages as
+//                 192 KB holds (4 at EN = 256 .. 9 at EN = 32), since the loop
+//                 is bound by the bytes in flight per SM
 //   warp 1        TMEM owner and MMA issuer: tcgen05.mma .kind::f16 (bf16 x
 //                 bf16 -> fp32), M = 128 tokens, N = EN experts, K = 16 per
 //                 instruction; two 256-column accumulators so that the
 //                 epilogue of one item overlaps the next item's main loop
 //   warps 2..5    epilogue: TMEM -> registers -> a swizzled smem tile ->
 //                 coalesced fp32 rows of the logits; then the item's token
-//                 tile completion counter is bumped (fence + atomic)
-//   warps 6..17   routing: take tokens one at a time from a global counter,
+//                 tile completion counter is bumped (fence + atomic).  With K
+//                 split S ways (few items: decode) each split writes a
+//                 partial tile and the last split of a (tile, chunk) to
+//                 finish sums the S partials in split order into the logits
+//   warps 6..15   routing: take tokens one at a time from a global counter,
 //                 wait (bounded) until every expert chunk of the token's tile
 //                 is written, route the token (route_dev.cuh)
 // The GEMM warps join the routing pool when their work runs out, so routing
@@ -27,15 +33,15 @@
 namespace kmoe {
 namespace {
 
-constexpr int kWarps = 18;
+constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kFirstRouteWarp = 6;
-constexpr int kStages = 3;
-constexpr int kATile = 128 * 128;           // 128 tokens x 64 bf16
-constexpr int kStage = kATile + 256 * 128;  // + up to 256 experts x 64 bf16
-constexpr int kStgOff = kStages * kStage;   // epilogue staging: 32 x 32 fp32 per warp
+constexpr int kMaxStages = 12;
+constexpr int kATile = 128 * 128;        // 128 tokens x 64 bf16 (the MMA's M = 128 rows)
+constexpr int kStageArea = 192 * 1024;   // stages of kATile + EN x 128 bytes, 1 KB aligned
+constexpr int kStgOff = kStageArea;      // epilogue staging: 32 x 32 fp32 per warp
 constexpr int kBarOff = kStgOff + 4 * 4096;
-constexpr int kBiasOff = kBarOff + 256;
+constexpr int kBiasOff = kBarOff + 512;
 constexpr int kIdxOff = kBiasOff + 4 * kMaxE;
 constexpr int kSmem = 1024 + kIdxOff + kWarps * 32 * 4;
 constexpr uint32_t kTmemCols = 512;  // two accumulators of up to 256 columns
@@ -70,28 +76,28 @@ template <int KPL>
 __device__ void route_pool(const RouterArgs& a, const float* s_b, int* s_idx, int lane) {
   int* next = a.sync;
   const int* tile_done = a.sync + 2;
-  const int need = a.plan.nch;
+  const int need = a.plan.nch;  // one count per expert chunk of the tile
   for (;;) {
     int t = 0;
     if (lane == 0) t = atomicAdd(next, 1);
     t = __shfl_sync(0xffffffffu, t, 0);
     if (t >= a.T) break;
+    // Every lane polls (an acquire load each) and the loop exits together:
+    // a wait run by one lane left the warp executing the routing diverged,
+    // at about three times the time per token.
     const int* c = tile_done + (t >> 7);
     int ready = 1;
-    if (lane == 0 && ld_acquire_gpu(c) < need) {
-      const uint64_t t0 = globaltimer_ns();
-      for (;;) {
-        __nanosleep(256);
-        if (ld_acquire_gpu(c) >= need) break;
-        if ((*reinterpret_cast<volatile uint32_t*>(a.err) & KMOE_DEVERR_TIMEOUT) ||
-            globaltimer_ns() - t0 > a.budget_ns) {
-          atomicOr(a.err, KMOE_DEVERR_TIMEOUT);
-          ready = 0;
-          break;
-        }
+    const uint64_t t0 = globaltimer_ns();
+    while (!__all_sync(0xffffffffu, ld_acquire_gpu(c) >= need)) {
+      __nanosleep(256);
+      const bool late = (*reinterpret_cast<volatile uint32_t*>(a.err) & KMOE_DEVERR_TIMEOUT) ||
+                        globaltimer_ns() - t0 > a.budget_ns;
+      if (__any_sync(0xffffffffu, late)) {
+        if (lane == 0) atomicOr(a.err, KMOE_DEVERR_TIMEOUT);
+        ready = 0;
+        break;
       }
     }
-    ready = __shfl_sync(0xffffffffu, ready, 0);
     int32_t* ids_row = a.ids + static_cast<size_t>(t) * a.k;
     float* w_row = a.wts + static_cast<size_t>(t) * a.k;
     if (!ready) {
@@ -101,7 +107,6 @@ __device__ void route_pool(const RouterArgs& a, const float* s_b, int* s_idx, in
       }
       continue;
     }
-    (void)ld_acquire_gpu(c);  // each lane's own acquire before it reads the logits
     route_token<KPL>(a.logits + static_cast<size_t>(t) * a.E, s_b, a.E, a.k, lane, ids_row, w_row, s_idx);
   }
 }
@@ -112,20 +117,24 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* acc_full = empty + kMaxStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // epilogue: last split
   float* s_b = reinterpret_cast<float*>(smem + kBiasOff);
   int* s_idx = reinterpret_cast<int*>(smem + kIdxOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < a.E; e += kThreads) s_b[e] = a.bias[e];
+  const int EN = a.plan.EN, nch = a.plan.nch, items = a.plan.items, S = a.plan.S, kper = a.plan.kper;
+  const int stride = (kATile + EN * 128 + 1023) & ~1023;  // bytes per pipeline stage
+  const int nst = kStageArea / stride < kMaxStages ? kStageArea / stride : kMaxStages;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -149,28 +158,38 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int EN = a.plan.EN, nch = a.plan.nch, items = a.plan.items;
   const int KS = a.H / 64;
   const uint64_t budget = a.budget_ns;
+  int* tile_done = a.sync + 2;
+  int* split_done = a.sync + 2 + a.plan.tiles;
+  // item it -> (token tile mt, expert chunk nc, K split sp), splits fastest
+  auto decode = [&](int it, int& mt, int& nc, int& sp) {
+    const int b = it / S;
+    sp = it - b * S;
+    mt = b / nch;
+    nc = b - mt * nch;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint32_t tx = kATile + static_cast<uint32_t>(EN) * 128;
+      const uint32_t tx = static_cast<uint32_t>(a.xrows + EN) * 128;
       const uint64_t pol_x = policy_evict_normal();
       const uint64_t pol_g = policy_evict_last();  // the gate weight is re-read by every token tile
       uint32_t n = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const int mt = it / nch, nc = it - mt * nch;
-        for (int ks = 0; ks < KS; ++ks, ++n) {
-          const int s = static_cast<int>(n % kStages);
-          const uint32_t ph = (n / kStages) & 1u;
+        int mt, nc, sp;
+        decode(it, mt, nc, sp);
+        const int ks1 = (sp + 1) * kper < KS ? (sp + 1) * kper : KS;
+        for (int ks = sp * kper; ks < ks1; ++ks, ++n) {
+          const int s = static_cast<int>(n % nst);
+          const uint32_t ph = (n / nst) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * kStage;
+          uint8_t* st = smem + s * stride;
           mbar_arrive_expect_tx(&full[s], tx);
           tma_load_2d(st, &maps.x, &full[s], 64 * ks, 128 * mt, pol_x);
           tma_load_2d(st + kATile, &maps.g, &full[s], 64 * ks, EN * nc, pol_g);
@@ -178,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
       }
       if (!ok) {
         // let the copies already issued land before the CTA can exit
-        const uint32_t first = n > static_cast<uint32_t>(kStages) ? n - kStages : 0u;
+        const uint32_t first = n > static_cast<uint32_t>(nst) ? n - nst : 0u;
         for (uint32_t i = first; i < n; ++i)
-          mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1u, 20000000ull, nullptr, nullptr);
+          mbar_wait_bounded(&full[i % nst], (i / nst) & 1u, 20000000ull, nullptr, nullptr);
       }
     }
     __syncwarp();
@@ -194,23 +213,26 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
       uint32_t ph = 0, li = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++li) {
+        int mt, nc, sp;
+        decode(it, mt, nc, sp);
+        const int nks = ((sp + 1) * kper < KS ? (sp + 1) * kper : KS) - sp * kper;
         const uint32_t acc = li & 1u;
         const uint32_t aph = (li >> 1) & 1u;
         if (!mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * 256u;
-        for (int ks = 0; ks < KS; ++ks) {
+        for (int ks = 0; ks < nks; ++ks) {
           if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t so = static_cast<uint64_t>(s) * (kStage >> 4);
+          const uint64_t so = static_cast<uint64_t>(s) * static_cast<uint64_t>(stride >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16(d, adesc0 + so + 2 * kk, bdesc0 + so + 2 * kk, idesc, (ks | kk) != 0);
           tc_commit(&empty[s]);
-          if (++s == kStages) {
+          if (++s == nst) {
             s = 0;
             ph ^= 1u;
           }
@@ -234,8 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
       ok = named_barrier_and(1, 128, ok && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const int mt = it / nch, nc = it - mt * nch;
+      int mt, nc, sp;
+      decode(it, mt, nc, sp);
       const int t0 = 128 * mt + 32 * q;
+      float* dst = S > 1 ? a.part + static_cast<size_t>(sp) * a.T * a.E : a.logits;
       for (int c0 = 0; c0 < EN; c0 += 32) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * 256u + c0, r);
@@ -254,17 +278,46 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
           const int rr = 4 * i + (lane >> 3);
           const int t = t0 + rr;
           const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + (((lane & 7) ^ (rr & 7)) << 2));
-          if (t < a.T && e0 < a.E) *reinterpret_cast<float4*>(a.logits + static_cast<size_t>(t) * a.E + e0) = v;
+          if (t < a.T && e0 < a.E) *reinterpret_cast<float4*>(dst + static_cast<size_t>(t) * a.E + e0) = v;
         }
         __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      // publish: every writer's stores before the tile's counter moves
+      // publish: every writer's stores before a counter moves
       __threadfence();
       named_barrier(1, 128);
-      if (warp == 2 && lane == 0) atomicAdd(a.sync + 2 + mt, 1);
+      if (S > 1) {
+        // the last of the S splits of (mt, nc) sums the partial tiles in split order
+        const int tid = threadIdx.x - 64;  // 0..127
+        if (tid == 0) *last_flag = atomicAdd(split_done + mt * nch + nc, 1) == S - 1;
+        named_barrier(1, 128);
+        const bool last = *last_flag != 0;
+        named_barrier(1, 128);  // the flag is read before the next item rewrites it
+        if (!last) continue;
+        __threadfence();
+        const int rows = a.T - 128 * mt < 128 ? a.T - 128 * mt : 128;
+        const int q4 = EN / 4;
+        for (int idx = tid; idx < rows * q4; idx += 128) {
+          const int r = idx / q4;
+          const int e = nc * EN + 4 * (idx - r * q4);
+          if (e >= a.E) continue;
+          const size_t off = static_cast<size_t>(128 * mt + r) * a.E + e;
+          float4 acc4 = __ldcg(reinterpret_cast<const float4*>(a.part + off));
+          for (int p = 1; p < S; ++p) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + static_cast<size_t>(p) * a.T * a.E + off));
+            acc4.x += v.x;
+            acc4.y += v.y;
+            acc4.z += v.z;
+            acc4.w += v.w;
+          }
+          *reinterpret_cast<float4*>(a.logits + off) = acc4;
+        }
+        __threadfence();
+        named_barrier(1, 128);
+      }
+      if (warp == 2 && lane == 0) atomicAdd(tile_done + mt, 1);
     }
   }
   route_pool<KPL>(a, s_b, s_idx + warp * 32, lane);
@@ -307,7 +360,9 @@ cudaError_t launch_kpl(const RouterMaps& maps, const RouterArgs& a, int sms, cud
 cudaError_t launch_router(const RouterMaps& maps, const RouterArgs& a, int sms, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   if (a.E % 4 != 0 || a.H % 64 != 0 || a.E > kMaxE || sms <= 0) return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(a.sync, 0, router_sync_bytes(a.T), st);
+  if (a.xrows != 32 && a.xrows != 64 && a.xrows != 128) return cudaErrorInvalidValue;
+  if (a.plan.S > 1 && a.part == nullptr) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(a.sync, 0, router_sync_bytes(a.plan), st);
   if (e != cudaSuccess) return e;
   if (a.E <= 64) return launch_kpl<2>(maps, a, sms, st);
   if (a.E <= 256) return launch_kpl<8>(maps, a, sms, st);

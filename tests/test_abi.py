@@ -66,8 +66,11 @@ def test_host_side_argument_errors(K):
         assert st in (1, 2)
     assert lib.kmoe_route(None, None, 4, 8, 9, None, None, None) == 1
     # the fused router: shapes, pointers, alignment and workspace are checked on the host
-    nr = K.kmoe_router_workspace_size(300)
-    assert nr == 256 + 256 and K.kmoe_router_workspace_size(-1) == 0
+    nr = K.kmoe_router_workspace_size(300, 128, 8)
+    assert nr >= 512 and K.kmoe_router_workspace_size(-1, 128, 8) == 0
+    assert K.kmoe_router_workspace_size(16, 96, 8) == 0 and K.kmoe_router_workspace_size(16, 128, 2000) == 0
+    # decode-sized routers split K: the partial sums are part of the workspace
+    assert K.kmoe_router_workspace_size(16, 7168, 896) > 5 * 16 * 896 * 4
     r = lib.kmoe_router
     assert r(16, 16, 16, 4, 128, 6, 2, 16, 16, 16, 256, nr, None) == 2      # E not a multiple of 4
     assert r(16, 16, 16, 4, 96, 8, 2, 16, 16, 16, 256, nr, None) == 2       # H not a multiple of 64

@@ -56,6 +56,25 @@ def test_route_ties_and_k_equals_e(K):
     assert np.array_equal(ids.cpu().numpy(), ref)
 
 
+def test_route_every_selection_path(K):
+    """Tokens built to take each of the kernel's three selection paths (the
+    lane-maximum bound, the radix select, the k rounds of arg-max) and edge
+    keys: NaN logits, a 40-way tie at the top, keys concentrated in one lane."""
+    E, k = 896, 16
+    rng = np.random.default_rng(4)
+    lg = rng.standard_normal((6, E)).astype(np.float32)
+    lg[1, ::32] = 5.0 + 0.01 * rng.standard_normal(E // 32).astype(np.float32)  # all in lane 0's experts
+    lg[2] = 0.0                                                                   # every key equal
+    lg[3, rng.choice(E, 40, replace=False)] = 4.0                                 # 40 equal keys on top
+    lg[4, rng.choice(E, 100, replace=False)] = np.nan                             # NaN -> never chosen
+    lg[5] = -30.0 + 0.001 * rng.standard_normal(E).astype(np.float32)             # tiny scores
+    for bias in (np.zeros(E, np.float32), (0.01 * rng.standard_normal(E)).astype(np.float32)):
+        ref, wref, _ = O.route(lg, bias, k)
+        ids, wts = K.kmoe_route(torch.from_numpy(lg).cuda(), torch.from_numpy(bias).cuda(), k)
+        assert np.array_equal(ids.cpu().numpy(), ref)
+        assert np.allclose(wts.cpu().numpy(), wref, rtol=1e-6)
+
+
 def _quant_check(K, xbits, fmt):
     x = torch.from_numpy(xbits.view(np.int16)).view(torch.bfloat16).cuda()
     codes, scales = K.kmoe_quantize_mx(x, fmt)
