@@ -111,11 +111,12 @@ __device__ __forceinline__ int stg_at(int r, int c) { return stg_unit(r, c >> 2)
 // (warp eq of the group reads lane quarter q).
 //   FC2: fp32 stores of rows 128*mt + lane to y of each column's routed slot.
 //   FC1: the group stages the chunk in smem (`stg`, 128 x 32 floats), then
-//        each math thread takes 16 consecutive intermediate columns of a token:
+//        each math thread takes UV (8 or 16) consecutive intermediate columns
+//        of a token:
 //        the activation (SiTU, or the SwiGLU control when a.act is set) of
 //        (gate, up) = (tile rows i, 64 + i), the MXFP8 scale of the 32-group
-//        (amax over two threads), E4M3 codes as one 16-byte store.
-template <bool FC1, int NCH>
+//        (amax over 32/UV threads), E4M3 codes as one 8- or 16-byte store.
+template <bool FC1, int NCH, int UV = 16>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk, int mt, uint32_t tacc, int c0,
                                                float* stg, int q, int eq, int lane, int grp, int skip_eq = -1,
                                                int heavy_eq = -1) {
@@ -143,12 +144,17 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
                       __uint_as_float(r[4 * u + 3]));
   }
   named_barrier(2 + grp, 128);
-  // 128 work units = (column, 32-group of the 64 intermediate indices, half),
-  // 16 consecutive intermediate values each; spread over the group's warps
-  // except warp `skip_eq` (the one that shares the MMA warp's scheduler); with
-  // three math warps, warp `heavy_eq` takes the extra pass.  Units u and u ^ 1
-  // (the two halves of a quantisation group) always fall in the same pass of
-  // the same warp.
+  // 32*64/UV work units = (column, UV consecutive intermediate values of the
+  // 64), spread over the group's warps except warp `skip_eq` (the one that
+  // shares the MMA warp's scheduler); with three math warps, the warps of the
+  // lowest ranks (warp `heavy_eq` first) take the extra pass.  The 32/UV units
+  // of a quantisation group sit on consecutive lanes of one warp in the same
+  // pass.  UV = 8 spreads the work more evenly over the three math warps (the
+  // busiest thread evaluates 24 values instead of 32): it pays where the main
+  // loop is short.
+  constexpr int kUnits = 32 * 64 / UV;
+  constexpr int kPer = 64 / UV;  // units per column
+  constexpr int kQ = 32 / UV;    // units per quantisation group
   if (eq != skip_eq) {
     int wm = eq;  // rank among the math warps (0 takes the extra pass)
     if (skip_eq >= 0) {
@@ -157,17 +163,16 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
       wm = r == h ? 0 : (r < h ? r + 1 : r);
     }
     const int stride = skip_eq >= 0 ? 96 : 128;
-    for (int t = wm * 32 + lane; t < 128; t += stride) {
-      const int cl = t >> 2;
-      const int gh = (t >> 1) & 1;
-      const int hh = t & 1;
+    for (int t = wm * 32 + lane; t < kUnits; t += stride) {
+      const int cl = t / kPer;
+      const int uu = t % kPer;
       const int col = c0 + cl;
-      const int i0 = 32 * gh + 16 * hh;
-      float act[16];
+      const int i0 = UV * uu;
+      float act[UV];
       float amax = 0.0f;
       if (a.act == 0) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < UV; ++i) {
           const float g = stg[stg_at(i0 + i, cl)];
           const float u = stg[stg_at(64 + i0 + i, cl)];
           act[i] = situ_f32(g, u, a.kg, a.ku, a.bb);
@@ -175,19 +180,20 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < UV; ++i) {
           const float g = stg[stg_at(i0 + i, cl)];
           const float u = stg[stg_at(64 + i0 + i, cl)];
           act[i] = swiglu_f32(g, u, a.sw_alpha, a.sw_beta, a.sw_limit);
           amax = fmaxf(amax, fabsf(act[i]));
         }
       }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the other half of the group
+#pragma unroll
+      for (int m = 1; m < kQ; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
       const int e = e4m3_scale_exp(amax);
       const float inv = exp2i(-e);
-      uint32_t w[4];
+      uint32_t w[UV / 4];
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
+      for (int k4 = 0; k4 < UV / 4; ++k4) {
         const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4] * inv, act[4 * k4 + 1] * inv),
                                                      __NV_SATFINITE, __NV_E4M3);
         const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4 + 2] * inv, act[4 * k4 + 3] * inv),
@@ -195,10 +201,13 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
         w[k4] = (lo & 0xFFFFu) | (hi << 16);
       }
       if (col < wk.n) {
-        *reinterpret_cast<uint4*>(a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-        if (hh == 0)
-          a.isf[tile_sf_offset(wk.tile, col, 2 * mt + gh, NCH, a.I / 128)] = static_cast<uint8_t>(e + 127);
+        uint8_t* dst = a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0;
+        if constexpr (UV == 16)
+          *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        else
+          *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+        if (uu % kQ == 0)
+          a.isf[tile_sf_offset(wk.tile, col, 2 * mt + uu / kQ, NCH, a.I / 128)] = static_cast<uint8_t>(e + 127);
       }
     }
   }

@@ -26,11 +26,12 @@
 
 namespace kmoe {
 
-template <bool FC1_, int STAGES_, bool DYN_>
+template <bool FC1_, int STAGES_, bool DYN_, int UV_ = 16>
 struct PairCfg {
   static constexpr bool FC1 = FC1_;
   static constexpr int STAGES = STAGES_;
   static constexpr bool DYN = DYN_;  // work items claimed dynamically (else pair p takes p, p + npairs, ...)
+  static constexpr int UV = UV_;     // FC1 activation values per epilogue work unit (8 or 16)
   static constexpr int KPS = 2;          // 128-wide K blocks per stage (8 pair MMAs)
   static constexpr int BN = 224;         // token rows per item (both CTAs)
   static constexpr int HALF = BN / 2;    // token rows loaded by each CTA
@@ -70,6 +71,12 @@ struct PairCfg {
 };
 
 constexpr int kRing = 8;  // work-item ring slots
+// FC1 with at most this many 128-wide K blocks (H = 3584: 28) has a main loop
+// short enough that the epilogue is on the critical path: its kernel uses
+// 8-value activation units, which spread the SiTU work more evenly over the
+// three math warps (FC1 3.54 -> 3.25 ms at H = 3584, I = 3072, T = 8192; at
+// H = 7168 the 16-value units are faster).
+constexpr int kShortKBlocks = 32;
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __grid_constant__ GemmMaps maps,
@@ -338,7 +345,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::BN;
       const int nchunk = (wk.n + 31) >> 5;
       for (int ci = grp; ci < nchunk; ci += C::NGRP)
-        epilogue_chunk<C::FC1, C::NCH>(a, wk, mt, tacc, ci * 32, stg, q, eq, lane, grp, kMmaSchedEq, kHeavyEq);
+        epilogue_chunk<C::FC1, C::NCH, C::UV>(a, wk, mt, tacc, ci * 32, stg, q, eq, lane, grp, kMmaSchedEq,
+                                              kHeavyEq);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -404,8 +412,9 @@ cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs&
   // FC1 claims items dynamically (in the fixed order its pairs finished up to
   // 4 % apart at H = 7168, and it is ahead at H = 3584 too); FC2's items do
   // better in the fixed order.
-  return fc1 ? launch_pair<PairCfg<true, 3, true>>(maps, a, sms, st)
-             : launch_pair<PairCfg<false, 3, false>>(maps, a, sms, st);
+  if (!fc1) return launch_pair<PairCfg<false, 3, false>>(maps, a, sms, st);
+  return a.KB <= kShortKBlocks ? launch_pair<PairCfg<true, 3, true, 8>>(maps, a, sms, st)
+                               : launch_pair<PairCfg<true, 3, true, 16>>(maps, a, sms, st);
 }
 
 }  // namespace kmoe
