@@ -137,7 +137,7 @@ int run_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, i
   if (!make_map(&m.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_bf16, H, T, static_cast<uint64_t>(H) * 2, 64,
                 static_cast<uint32_t>(a.xrows)) ||
       !make_map(&m.g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_gate_bf16, H, E, static_cast<uint64_t>(H) * 2, 64,
-                static_cast<uint32_t>(a.plan.EN)))
+                static_cast<uint32_t>(a.plan.pair ? a.plan.EN / 2 : a.plan.EN)))
     return KMOE_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return KMOE_ERR_CUDA;

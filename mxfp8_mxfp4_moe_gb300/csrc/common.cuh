@@ -41,13 +41,25 @@ struct RouterPlan {
   int tiles;  // token tiles: ceil(T / 128)
   int S;      // K splits
   int kper;   // 64-wide K steps per split (the last split may have fewer)
-  int items;  // tiles * nch * S
+  int items;  // tiles * nch * S; CTA pairs: ceil(tiles / 2) * nch
+  int pair;   // 1: items run on CTA pairs (two token tiles, M = 256, EN / 2 gate rows per CTA)
 };
 
-// EN minimises (rounds of items over 152 SMs) x (MMA time per K step,
-// proportional to EN above ~112 columns, flat below); ties go to the smaller
-// EN (more SMs streaming the gate weight).  Fewer than 76 items: K is split
-// so that about 152 items run, each with at least 8 K steps.
+// Estimated cycles of one 64-wide K step of an item: the larger of its loads
+// (bytes per SM at ~49 B per cycle, the bytes in flight over the load latency)
+// and its 4 MMAs (EN / 2 cycles each, at least ~54).
+__host__ inline long long router_step_cycles(int EN, bool pair) {
+  const long long bytes = 16384 + (pair ? 64LL : 128LL) * EN;
+  const long long load = bytes / 49;
+  const long long mma = 4LL * (EN / 2 > 54 ? EN / 2 : 54);
+  return load > mma ? load : mma;
+}
+
+// One CTA per item: EN minimises (rounds of items over 152 SMs) x (MMA time
+// per K step, proportional to EN above ~112 columns, flat below); ties go to
+// the smaller EN (more SMs streaming the gate weight).  Fewer than 76 items:
+// K is split so that about 152 items run, each with at least 8 K steps.
+// Enough token tiles: CTA pairs if the step estimate favours them.
 __host__ inline RouterPlan plan_router(int T, int H, int E) {
   constexpr int kSlots = 152;
   RouterPlan best{};
@@ -60,10 +72,28 @@ __host__ inline RouterPlan plan_router(int T, int H, int E) {
     const long long cost = rounds * (en > 112 ? en : 112);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
-      best = RouterPlan{en, nch, tiles, 1, 0, static_cast<int>(items)};
+      best = RouterPlan{en, nch, tiles, 1, 0, static_cast<int>(items), 0};
     }
   }
   const int KS = H / 64;
+  // CTA pairs: each SM moves its 128 token rows and half of the EN gate rows
+  // per K step for the same MMA work; taken when the estimate is 10 % better
+  if (tiles >= 2 && best.items >= kSlots / 2) {
+    const long long single = ((best.items + kSlots - 1) / kSlots) * router_step_cycles(best.EN, false);
+    const int tpairs = (tiles + 1) / 2;
+    RouterPlan pb{};
+    long long pcost = -1;
+    for (int en = 32; en <= 256; en += 32) {
+      const int nch = (E + en - 1) / en;
+      const long long items = static_cast<long long>(tpairs) * nch;
+      const long long cost = ((items + kSlots / 2 - 1) / (kSlots / 2)) * router_step_cycles(en, true);
+      if (pcost < 0 || cost < pcost) {
+        pcost = cost;
+        pb = RouterPlan{en, nch, tiles, 1, KS, static_cast<int>(items), 1};
+      }
+    }
+    if (10 * pcost < 9 * single) return pb;
+  }
   const int base = best.items;
   int S = 1;
   if (base > 0 && base < kSlots / 2) {

@@ -64,10 +64,51 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// The CTA-pair form (M = 256): CTA r supplies A rows [128r, 128r+128) and B
+// rows [rN/2, (r+1)N/2) from its own shared memory; each CTA's TMEM gets its
+// 128 x N accumulator.  Issued by the even CTA.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// One warp's 32 token rows of an item's accumulator (TMEM columns
+// [0, EN) at `tacc`, lane quarter included) to fp32 logits rows t0..t0+31,
+// columns e_base..e_base+EN-1 of dst [T, E]: TMEM -> registers -> a
+// swizzled 32 x 32 smem tile (row `lane`'s 16-byte unit u at u ^ (lane & 7))
+// -> 8 lanes per row, 128 contiguous bytes, 4 rows per store.
+__device__ __forceinline__ void store_logit_tile(uint32_t tacc, int EN, float* stg, int lane, int t0, int e_base,
+                                                 int T, int E, float* dst) {
+  for (int c0 = 0; c0 < EN; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tacc + c0, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) << 2)) =
+          make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]), __uint_as_float(r[4 * u + 2]),
+                      __uint_as_float(r[4 * u + 3]));
+    __syncwarp();
+    const int e0 = e_base + c0 + 4 * (lane & 7);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3);
+      const int t = t0 + rr;
+      const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + (((lane & 7) ^ (rr & 7)) << 2));
+      if (t < T && e0 < E) *reinterpret_cast<float4*>(dst + static_cast<size_t>(t) * E + e0) = v;
+    }
+    __syncwarp();
+  }
 }
 
 // Routing warps: tokens are handed out in increasing order, so the first
@@ -260,28 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
       decode(it, mt, nc, sp);
       const int t0 = 128 * mt + 32 * q;
       float* dst = S > 1 ? a.part + static_cast<size_t>(sp) * a.T * a.E : a.logits;
-      for (int c0 = 0; c0 < EN; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * 256u + c0, r);
-        tmem_ld_wait();
-        // row `lane` of the 32 x 32 tile; its 16-byte unit u goes to u ^ (lane & 7)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) << 2)) =
-              make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]), __uint_as_float(r[4 * u + 2]),
-                          __uint_as_float(r[4 * u + 3]));
-        __syncwarp();
-        // 8 lanes per token row (128 contiguous bytes), 4 rows per store
-        const int e0 = nc * EN + c0 + 4 * (lane & 7);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + (lane >> 3);
-          const int t = t0 + rr;
-          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + (((lane & 7) ^ (rr & 7)) << 2));
-          if (t < a.T && e0 < a.E) *reinterpret_cast<float4*>(dst + static_cast<size_t>(t) * a.E + e0) = v;
-        }
-        __syncwarp();
-      }
+      store_logit_tile(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * 256u, EN, stg, lane, t0, nc * EN, a.T,
+                       a.E, dst);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -330,6 +351,220 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
   }
 }
 
+// The gate GEMM on CTA pairs (plan.pair): a cluster of two CTAs runs item
+// (token-tile pair tp, expert chunk nc) as tcgen05.mma.cta_group::2 of M = 256
+// tokens (CTA r: token tile 2tp + r) by N = EN experts (CTA r holds gate rows
+// [EN nc + r EN/2, +EN/2)); each CTA's TMEM receives its own 128 x EN
+// accumulator, which its epilogue writes as logits rows of its token tile.
+// Both CTAs' loads complete on the even CTA's full barrier (TMA
+// .cta_group::2); the even CTA's MMA commits arrive on both CTAs' empty and
+// acc_full barriers; acc_empty of the even CTA counts both CTAs' epilogue
+// warps.  Routing as in router_kernel.  No K split (pairs are used only when
+// there are enough token tiles).
+template <int KPL>
+__global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_constant__ RouterMaps maps,
+                                                                  const RouterArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* acc_full = empty + kMaxStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_b = reinterpret_cast<float*>(smem + kBiasOff);
+  int* s_idx = reinterpret_cast<int*>(smem + kIdxOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool lead = rank == 0;
+  for (int e = threadIdx.x; e < a.E; e += kThreads) s_b[e] = a.bias[e];
+  const int EN = a.plan.EN, nch = a.plan.nch, items = a.plan.items, tiles = a.plan.tiles;
+  const int half = EN / 2;
+  const int stride = (kATile + half * 128 + 1023) & ~1023;  // bytes per pipeline stage
+  const int nst = kStageArea / stride < kMaxStages ? kStageArea / stride : kMaxStages;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(&full[s], 1);   // the even CTA's producer (plus both CTAs' bytes)
+      mbar_init(&empty[s], 1);  // the pair MMA's commit (multicast)
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);  // the epilogue warps of both CTAs
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.x);
+    prefetch_tmap(&maps.g);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int KS = a.H / 64;
+  const uint64_t budget = a.budget_ns;
+  int* tile_done = a.sync + 2;
+  const int pairi = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producers (both CTAs)
+    if (lane == 0) {
+      const uint32_t tx2 = 2u * static_cast<uint32_t>(kATile + half * 128);
+      const uint64_t pol_x = policy_evict_normal();
+      const uint64_t pol_g = policy_evict_last();
+      const uint32_t lead_full = cluster_map(full, 0);
+      uint32_t n = 0;
+      bool ok = true;
+      for (int it = pairi; it < items && ok; it += npairs) {
+        const int tp = it / nch, nc = it - tp * nch;
+        const int mt = 2 * tp + static_cast<int>(rank);
+        const int grow = EN * nc + static_cast<int>(rank) * half;
+        for (int ks = 0; ks < KS; ++ks, ++n) {
+          const int s = static_cast<int>(n % nst);
+          const uint32_t ph = (n / nst) & 1u;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * stride;
+          const uint32_t bar = lead_full + 8u * static_cast<uint32_t>(s);
+          if (lead) mbar_arrive_expect_tx(&full[s], tx2);
+          tma_load_2d_pair(st, &maps.x, bar, 64 * ks, 128 * mt, pol_x);
+          tma_load_2d_pair(st + kATile, &maps.g, bar, 64 * ks, grow, pol_g);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA can exit
+        if (lead) {
+          const uint32_t first = n > static_cast<uint32_t>(nst) ? n - nst : 0u;
+          for (uint32_t i = first; i < n; ++i)
+            mbar_wait_bounded(&full[i % nst], (i / nst) & 1u, 20000000ull, nullptr, nullptr);
+        } else {
+          spin_ns(100000ull);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && lead) {
+      const uint32_t idesc = idesc_bf16(256, static_cast<uint32_t>(EN));
+      const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
+      const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + kATile));
+      int s = 0;
+      uint32_t ph = 0, li = 0;
+      bool ok = true;
+      for (int it = pairi; it < items && ok; it += npairs, ++li) {
+        const uint32_t acc = li & 1u;
+        if (!mbar_wait_bounded<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * 256u;
+        for (int ks = 0; ks < KS; ++ks) {
+          if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = static_cast<uint64_t>(s) * static_cast<uint64_t>(stride >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_pair(d, adesc0 + so + 2 * kk, bdesc0 + so + 2 * kk, idesc, (ks | kk) != 0);
+          tc_commit_pair(&empty[s]);
+          if (++s == nst) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(&acc_full[acc]);
+      }
+      tc_commit_pair(done);
+      mbar_wait_bounded(done, 0, budget, a.err, nullptr);
+    }
+    __syncwarp();
+  } else if (warp < kFirstRouteWarp) {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    float* stg = reinterpret_cast<float*>(smem + kStgOff) + (warp - 2) * 1024;
+    const uint32_t lead_acc_empty = cluster_map(acc_empty, 0);
+    uint32_t li = 0;
+    for (int it = pairi; it < items; it += npairs, ++li) {
+      const uint32_t acc = li & 1u;
+      bool ok = mbar_wait_bounded(&acc_full[acc], (li >> 1) & 1u, budget, a.err, abort_flag);
+      ok = named_barrier_and(1, 128, ok && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int tp = it / nch, nc = it - tp * nch;
+      const int mt = 2 * tp + static_cast<int>(rank);
+      store_logit_tile(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * 256u, EN, stg, lane, 128 * mt + 32 * q,
+                       nc * EN, a.T, a.E, a.logits);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (lead)
+          mbar_arrive(&acc_empty[acc]);
+        else
+          mbar_arrive_remote(lead_acc_empty + 8u * acc);
+      }
+      // publish: every writer's stores before the tile's counter moves
+      __threadfence();
+      named_barrier(1, 128);
+      if (warp == 2 && lane == 0 && mt < tiles) atomicAdd(tile_done + mt, 1);
+    }
+  }
+  route_pool<KPL>(a, s_b, s_idx + warp * 32, lane);
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no MMA of the pair and no remote arrive is outstanding past here
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+template <int KPL>
+cudaError_t launch_pair_kpl(const RouterMaps& maps, const RouterArgs& a, int sms, cudaStream_t st) {
+  static int pairs = 0;  // co-resident clusters of two (per instantiation; idempotent)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeCooperative;  // the routing warps wait on other CTAs' tiles
+  at[1].val.cooperative = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  if (pairs == 0) {
+    cudaError_t e =
+        cudaFuncSetAttribute(router_pair_kernel<KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, router_pair_kernel<KPL>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    pairs = n < sms / 2 ? n : sms / 2;
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  return cudaLaunchKernelEx(&cfg, router_pair_kernel<KPL>, maps, a);
+}
+
 template <int KPL>
 cudaError_t launch_kpl(const RouterMaps& maps, const RouterArgs& a, int sms, cudaStream_t st) {
   static int ready = 0;  // attribute set and occupancy checked (per instantiation; idempotent)
@@ -364,6 +599,12 @@ cudaError_t launch_router(const RouterMaps& maps, const RouterArgs& a, int sms, 
   if (a.plan.S > 1 && a.part == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(a.sync, 0, router_sync_bytes(a.plan), st);
   if (e != cudaSuccess) return e;
+  if (a.plan.pair) {
+    if (a.xrows != 128 || a.plan.S != 1) return cudaErrorInvalidValue;
+    if (a.E <= 64) return launch_pair_kpl<2>(maps, a, sms, st);
+    if (a.E <= 256) return launch_pair_kpl<8>(maps, a, sms, st);
+    return launch_pair_kpl<32>(maps, a, sms, st);
+  }
   if (a.E <= 64) return launch_kpl<2>(maps, a, sms, st);
   if (a.E <= 256) return launch_kpl<8>(maps, a, sms, st);
   return launch_kpl<32>(maps, a, sms, st);

@@ -30,6 +30,9 @@ CASES = {
     "tiny_k_eq_E": W.WORKLOADS["tiny"].with_(name="tiny_k8", k=8),
     "T1": W.WORKLOADS["tiny"].with_(name="router_T1", T=1, H=512, E=64, k=4),
     "ragged": RAGGED,
+    # CTA pairs (prefill-sized plan) with an odd number of token tiles (the
+    # last pair's second CTA has no tokens) and a partial last expert chunk
+    "pair_odd_tiles": W.WORKLOADS["tiny"].with_(name="router_pair_odd", T=2100, H=512, E=900, k=16),
     "reduced": W.WORKLOADS["reduced"],
     "decode": W.WORKLOADS["decode"],
     "skewed": W.WORKLOADS["skewed"],
