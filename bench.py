@@ -270,6 +270,32 @@ def time_layer(layer, steps, warmup, dist, device, clocks=None):
     return total_ms, clk
 
 
+def time_graph(layer, steps):
+    """The layer's forward captured once into a CUDA graph and replayed
+    `steps` times back to back (no host launch work between kernels);
+    microseconds per forward."""
+    import torch
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        layer.forward()  # warm-up on the capture stream
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        layer.forward()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    return 1000.0 * s.elapsed_time(e) / steps
+
+
 def time_stages(layer, steps):
     """Per-stage durations from the stage events, averaged over `steps` forwards."""
     import torch
@@ -509,6 +535,8 @@ def run_ours(args):
     d_fc1_gbs = touched * per_expert_w13 / (d_stages[3] / 1e3) / 1e9
     d_layer_bytes = touched * per_expert_all + 2 * wd.T * wd.H * 2 + 4 * wd.T * wd.E
     d_layer_gbs = d_layer_bytes / (d_us / 1e6) / 1e9
+    d_graph_us = time_graph(dl, max(args.steps, 20))
+    dl.check()
 
     del dl
 
@@ -621,7 +649,8 @@ def run_ours(args):
             "swiglu_control": swiglu_control,
             "router": router,
             "decode": {"workload": "Kimi-K3 MoE layer decode T=16 H=7168 I=3584 E=896 top-16",
-                       "us_per_layer": d_us, "touched_experts": touched, "layer_GBs": d_layer_gbs,
+                       "us_per_layer": d_us, "us_per_layer_cuda_graph": d_graph_us,
+                       "touched_experts": touched, "layer_GBs": d_layer_gbs,
                        "layer_hbm_frac": d_layer_gbs / peaks["hbm_gbs"],
                        "stages_us": {n: 1000 * v for n, v in zip(K.STAGE_NAMES, d_stages)},
                        "roofline": {"bound": "hbm", "kernel": "FC1 grouped GEMM", "achieved": d_fc1_gbs,
