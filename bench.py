@@ -23,6 +23,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -89,7 +90,9 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.t0 = self.t1 = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples go to a scratch directory (the summary goes into the JSON line)
+        d = os.environ.get("KMOE_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"kmoe_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
