@@ -465,27 +465,6 @@ def oracle_slot_sample(w: W.Workload, budget_s: float, seed: int, pre):
     return (pairs / w.k) / done_s, pairs / w.k, done_s, os.cpu_count()
 
 
-def oracle_sample(w: W.Workload, budget_s: float = 12.0, seed: int = 7, pre=None):
-    """Time the float64 oracle (as it stands) on a bounded token sample of the
-    workload; returns (tokens/s, tokens, seconds, threads)."""
-    from oracle import moe as O
-    s, ids, _ = pre if pre is not None else oracle_inputs(w)
-    rng = np.random.default_rng(seed)
-    order = rng.permutation(w.T)
-    n = 1
-    done_tok, done_s = 0, 0.0
-    while done_s < budget_s and done_tok < w.T:
-        tokens = np.sort(order[done_tok:done_tok + n])
-        used = sorted(set(int(e) for e in ids[tokens].ravel()))
-        wts = W.gen_expert_weights_np(w, used)          # data generation: outside the timed region
-        t0 = time.perf_counter()
-        O.forward(w, s["x"], s["logits"], s["bias"], wts, experts_host=used, tokens=tokens, ids=None)
-        done_s += time.perf_counter() - t0
-        done_tok += len(tokens)
-        n = min(2 * n, 8)
-    return done_tok / done_s, done_tok, done_s, os.cpu_count()
-
-
 # ----------------------------------------------------------------------------- main
 def run_reference(args):
     ws, rank, _ = dist_env()
@@ -648,10 +627,12 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tps, ntok, secs, cores = oracle_sample(wp, budget_s=args.cpu_budget_s)
+        tps, ntok, secs, cores = oracle_slot_sample(wp, args.cpu_budget_s, 0, oracle_inputs(wp))
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{ntok} random tokens of the T=8192 layer ({secs:.1f} s of float64 oracle work: "
-                         f"routing of all tokens, then quantise/FC1/SiTU/requant/FC2/combine for the sample)"}
+               "sample": f"{round(ntok * wp.k)} random (token, expert slot) pairs of the T=8192 layer = "
+                         f"{ntok:.3g} token equivalents ({secs:.1f} s of float64 oracle work: quantise, FC1, "
+                         f"SiTU, requantise, FC2, combine of one slot per pair; routing of all tokens done once "
+                         f"before)"}
 
     if rank == 0:
         line = {
