@@ -14,6 +14,7 @@
  * Layout conventions (all row-major, contiguous, no strides):
  *   bf16 activations x      [T, H]
  *   router logits           [T, E] float
+ *   router (gate) weight    [E, H] bf16 (kmoe_router, kmoe_forward_router)
  *   correction bias         [E] float
  *   w13 codes               [E, 2I, H/2] uint8, two E2M1 codes per byte
  *                           (element 2j in the low nibble); rows [0, I) are
@@ -30,7 +31,8 @@
  *     the SiTU formula with situ_beta = 4 and situ_linear_beta = 25, the
  *     gated width rule (FC1 = 2 x FC2 K), the NaN/Inf decision record
  *     (saturating-finite MXFP8, no 0xFF scale), and the non-fused,
- *     deterministic finalize.
+ *     deterministic finalize; the gate's logits that TopK consumes (the
+ *     fused router) and the SwiGLU control group's parameters.
  *   - Kimi-K3 MoE path analysis page (SM100 section): MXFP8 pre-dispatch
  *     quantisation (per-32 absmax -> UE8M0 -> E4M3, four scale bytes per
  *     int32), weight/scale re-layout at load time for TMEM-staged scales,
@@ -115,7 +117,7 @@ typedef struct kmoe_ws_layout {
   size_t slot_of_row;  /* int32 [R] slot t*k+j of each expert-sorted row */
   size_t xq;           /* uint8 [R, H] E4M3 codes of x, expert-sorted */
   size_t xsf;          /* uint8 tile-layout UE8M0 scales of xq (see kmoe_tile_sf_offset) */
-  size_t iq;           /* uint8 [R, I] E4M3 codes of SiTU(FC1), expert-sorted */
+  size_t iq;           /* uint8 [R, I] E4M3 codes of the FC1 activation, expert-sorted */
   size_t isf;          /* uint8 tile-layout UE8M0 scales of iq */
   size_t y;            /* float [T*k, H] per-slot FC2 outputs (slot order) */
   int tile_rows;       /* rows per token tile (BN) chosen for these parameters */
@@ -151,8 +153,9 @@ int kmoe_route(const float* logits, const float* bias, int T, int E, int k, int3
  *   (0 for invalid sizes), 256-byte aligned, caller-owned: counters and, when
  *   few token tiles leave SMs idle (decode), the partial sums of a split K;
  *   its first word is the device error word (read it with
- *   kmoe_device_error).  The call launches one CTA per SM as a
- *   cooperative launch (all co-resident), so it fails with KMOE_ERR_CUDA if
+ *   kmoe_device_error).  The call launches one CTA per SM (in clusters of
+ *   two, M = 256 tensor-core pairs, when there are enough 128-token tiles) as
+ *   a cooperative launch (all co-resident), so it fails with KMOE_ERR_CUDA if
  *   the device cannot host them all at once.  Every device wait is bounded;
  *   a token whose logits did not arrive in time is left masked (ids -1,
  *   weights 0) and the timeout bit is set. */
@@ -197,8 +200,9 @@ int kmoe_prepare_weights(const kmoe_params* p, const uint8_t* w13, const uint8_t
 
 /* The routed-expert MoE forward:
  *   route (unless topk_ids/topk_w are given) -> MXFP8-quantise x ->
- *   expert-sorted permutation -> FC1 (x . w13^T, gate and up) -> SiTU ->
- *   MXFP8 requantise -> FC2 (. w2^T) -> out[t] = bf16(rsf * sum_j w_j y_j)
+ *   expert-sorted permutation -> FC1 (x . w13^T, gate and up) -> SiTU (or
+ *   the SwiGLU control with KMOE_FLAG_SWIGLU) -> MXFP8 requantise -> FC2
+ *   (. w2^T) -> out[t] = bf16(rsf * sum_j w_j y_j)
  *   with slots summed in order j = 0..k-1 in fp32 (deterministic).
  * x [T, H] bf16 (16-byte aligned); logits/bias as kmoe_route (ignored when
  * topk_ids is given); w13_k/w2_k from kmoe_prepare_weights (256-byte
