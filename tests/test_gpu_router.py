@@ -37,6 +37,9 @@ CASES = {
     "decode": W.WORKLOADS["decode"],
     "skewed": W.WORKLOADS["skewed"],
     "prefill": W.WORKLOADS["prefill"],
+    # the real checkpoint's hidden size (H = 3584): CTA pairs at T = 8192, split K at T = 16
+    "real_prefill": W.NEXT_WORKLOADS["real_prefill"],
+    "real_decode": W.NEXT_WORKLOADS["real_decode"],
 }
 
 
@@ -153,11 +156,12 @@ def test_router_deterministic_and_graph_replay(K):
     assert K.kmoe_device_error(ws)[0] == 0
 
 
-@pytest.mark.parametrize("name,sample", [("decode", 3), ("prefill", 2)])
-def test_forward_with_fused_router(K, name, sample):
+@pytest.mark.parametrize("name,sample,activation", [("decode", 3, "situ"), ("prefill", 2, "situ"),
+                                                    ("decode", 3, "swiglu")])
+def test_forward_with_fused_router(K, name, sample, activation):
     """kmoe_forward_router = kmoe_forward on the router's logits, bit for bit;
     sampled tokens against the oracle routed on those logits."""
-    w = W.WORKLOADS[name]
+    w = W.WORKLOADS[name].with_(activation=activation)
     s = W.gen_small_inputs(w)
     wt = device_weights(w)
     p = params(w)
@@ -181,4 +185,4 @@ def test_forward_with_fused_router(K, name, sample):
     used = sorted(set(int(e) for e in ids_k[tokens].ravel()))
     ref = O.forward(w, s["x"], None, None, W.gen_expert_weights_np(w, used), experts_host=used, tokens=tokens,
                     ids=ids_k, topk_w=w_k)
-    assert_output_parity(out_r[torch.from_numpy(tokens).cuda()], ref["out"], name + "_router")
+    assert_output_parity(out_r[torch.from_numpy(tokens).cuda()], ref["out"], f"{name}_{activation}_router")
