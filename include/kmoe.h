@@ -10,6 +10,10 @@
  * back with kmoe_device_error().  Argument errors are reported before
  * anything is enqueued.  All calls are safe to capture in a CUDA graph
  * (fixed grids, device-side counts, no host reads of device data).
+ * An empty batch (T = 0, or rows = 0 for kmoe_quantize_mx) is valid
+ * everywhere: after the size checks the call returns KMOE_OK having
+ * enqueued nothing, so the outputs and the workspace (its error word
+ * included) keep their contents, and null data pointers are accepted.
  *
  * Layout conventions (all row-major, contiguous, no strides):
  *   bf16 activations x      [T, H]

@@ -40,6 +40,8 @@ CASES = {
     # the real checkpoint's hidden size (H = 3584): CTA pairs at T = 8192, split K at T = 16
     "real_prefill": W.NEXT_WORKLOADS["real_prefill"],
     "real_decode": W.NEXT_WORKLOADS["real_decode"],
+    # the largest expert count and top-k the routing supports
+    "max_e_k": W.WORKLOADS["tiny"].with_(name="router_max_e_k", T=300, H=256, E=1024, k=32),
 }
 
 

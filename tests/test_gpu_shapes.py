@@ -7,7 +7,9 @@ every token against the float64 oracle:
 - a single expert (E = k = 1, every row to it);
 - k = 32 (the largest top-k), 64-row tiles;
 - E = 37 (no power of two), k = 5;
-- a three-token decode batch (32-row tiles).
+- a three-token decode batch (32-row tiles);
+- the largest expert count and top-k the routing supports (E = 1024,
+  k = 32), 32-row tiles.
 The stage checks (routing, permutation, codes and scales bit-exact) are those
 of test_gpu_forward."""
 import numpy as np
@@ -26,6 +28,7 @@ SHAPES = {
     "k32": (BASE.with_(name="k32", T=64, H=256, I=128, E=64, k=32), 64),
     "e37_k5": (BASE.with_(name="e37_k5", T=333, H=256, I=256, E=37, k=5), 64),
     "decode3": (BASE.with_(name="decode3", T=3, H=512, I=256, E=64, k=4), 32),
+    "max_e_k": (BASE.with_(name="max_e_k", T=64, H=256, I=128, E=1024, k=32), 32),
 }
 
 
