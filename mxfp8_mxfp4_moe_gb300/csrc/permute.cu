@@ -8,6 +8,8 @@
 //          and the block's per-expert counts.
 //   pass 2 (scan_kernel, one block): per-expert totals, prefix over blocks,
 //          segment starts and tile starts (prefix of ceil(count/BN)).
+// Batches of at most kRankChunk slots (decode) take both passes in one block
+// (permute_small_kernel): one launch, the counts staying in shared memory.
 // The final row of slot s is seg_start[e] + chunk_prefix[block][e] + rank[s];
 // it is computed where the row is written (the quantise-scatter kernel).
 #include "common.cuh"
@@ -104,15 +106,107 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ chunk_
   }
 }
 
+// Single block of kRankChunk threads for R <= kRankChunk and E <= kMaxE: the
+// ranks of rank_kernel's first block (slot s on thread s) and the scans of
+// scan_kernel (expert e on thread e) over the counts in shared memory.  The
+// one chunk's exclusive prefix is 0.
+__global__ void __launch_bounds__(kRankChunk) permute_small_kernel(const int32_t* __restrict__ ids, int R, int E,
+                                                                   int BN, int32_t* __restrict__ rank,
+                                                                   int32_t* __restrict__ chunk_prefix,
+                                                                   int32_t* __restrict__ counts,
+                                                                   int32_t* __restrict__ seg_start,
+                                                                   int32_t* __restrict__ tile_start,
+                                                                   uint32_t* __restrict__ err) {
+  static_assert(kRankChunk == 1024 && kMaxE <= kRankChunk, "one slot and one expert per thread, 32 warps");
+  __shared__ int cnt[kMaxE];
+  __shared__ int w_rows[32], w_tiles[32];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  // stable ranks: warps in order, lanes in order inside a warp
+  const int s = threadIdx.x;
+  int id = s < R ? ids[s] : -1;
+  if (id >= E) {
+    atomicOr(err, 2u);  // KMOE_DEVERR_BOUNDS: an expert id out of range (treated as masked)
+    id = -1;
+  }
+  const bool valid = id >= 0;
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? id : -1);
+  const unsigned lower = peers & ((1u << lane) - 1u);
+  int my = -1;
+  const int nw = (R + 31) >> 5;  // warps that hold slots (the same bound for every thread)
+  for (int w = 0; w < nw; ++w) {
+    int base = 0;
+    if (warp == w && valid) base = cnt[id];
+    __syncwarp();
+    if (warp == w && valid) {
+      my = base + __popc(lower);
+      if (lower == 0) cnt[id] = base + __popc(peers);
+    }
+    __syncthreads();
+  }
+  if (s < R) rank[s] = my;
+  // exclusive prefixes of rows and tiles in expert order
+  const int e = threadIdx.x;
+  const int c = e < E ? cnt[e] : 0;
+  const int t = (c + BN - 1) / BN;
+  if (e < E) {
+    counts[e] = c;
+    chunk_prefix[e] = 0;
+  }
+  int ir = c, it = t;  // inclusive within the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int vr = __shfl_up_sync(0xffffffffu, ir, off);
+    const int vt = __shfl_up_sync(0xffffffffu, it, off);
+    if (lane >= off) {
+      ir += vr;
+      it += vt;
+    }
+  }
+  if (lane == 31) {
+    w_rows[warp] = ir;
+    w_tiles[warp] = it;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int wr = w_rows[lane], wt = w_tiles[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int vr = __shfl_up_sync(0xffffffffu, wr, off);
+      const int vt = __shfl_up_sync(0xffffffffu, wt, off);
+      if (lane >= off) {
+        wr += vr;
+        wt += vt;
+      }
+    }
+    w_rows[lane] = wr;  // inclusive over warps
+    w_tiles[lane] = wt;
+  }
+  __syncthreads();
+  if (e < E) {
+    seg_start[e] = (warp > 0 ? w_rows[warp - 1] : 0) + ir - c;
+    tile_start[e] = (warp > 0 ? w_tiles[warp - 1] : 0) + it - t;
+  }
+  if (threadIdx.x == 0) {
+    seg_start[E] = w_rows[31];
+    tile_start[E] = w_tiles[31];
+  }
+}
+
 cudaError_t launch_permute(const int32_t* ids, int R, int E, int BN, int32_t* rank, int32_t* chunk_prefix,
                            int32_t* counts, int32_t* seg_start, int32_t* tile_start, uint32_t* err,
                            cudaStream_t st) {
   const int nchunk = (R + kRankChunk - 1) / kRankChunk;
-  if (nchunk > 0) {
-    rank_kernel<<<nchunk, kRankChunk, E * sizeof(int), st>>>(ids, R, E, rank, chunk_prefix, err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  if (nchunk <= 1) {
+    permute_small_kernel<<<1, kRankChunk, 0, st>>>(ids, R, E, BN, rank, chunk_prefix, counts, seg_start, tile_start,
+                                                   err);
+    return cudaGetLastError();
   }
+  rank_kernel<<<nchunk, kRankChunk, E * sizeof(int), st>>>(ids, R, E, rank, chunk_prefix, err);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   scan_kernel<<<1, 1024, 0, st>>>(chunk_prefix, nchunk, E, BN, counts, seg_start, tile_start);
   return cudaGetLastError();
 }
