@@ -121,15 +121,38 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev(t, name, dtype=None):
+def _arg(t, name, dtype=None, shape=None, min_bytes=None):
+    """Checks a caller tensor before its pointer reaches the library, which
+    sees no sizes: dtype, exact shape or a minimum size in bytes, and
+    contiguity.  None passes (optional arguments).  Each entry point checks
+    every argument this way, then that all of them live on the GPU (_gpu)."""
     if t is None:
         return
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous (strided input is rejected, not copied)")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if min_bytes is not None and _nbytes(t) < min_bytes:
+        raise ValueError(f"{name} holds {_nbytes(t)} bytes, needs at least {min_bytes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (strided input is rejected, not copied)")
+
+
+def _gpu(**tensors):
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _rows(t, name, ncols_name):
+    """(rows, cols) of a 2-D argument."""
+    if t is None or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D tensor [rows, {ncols_name}]")
+    return t.shape
 
 
 KMOE_FLAG_SWIGLU = 1
@@ -164,9 +187,12 @@ def kmoe_workspace_layout(p: kmoe_params) -> kmoe_ws_layout:
 
 
 def kmoe_route(logits, bias, k, topk_ids=None, topk_w=None, stream=None):
-    _dev(logits, "logits", torch.float32)
-    _dev(bias, "bias", torch.float32)
-    T, E = logits.shape
+    T, E = _rows(logits, "logits", "E")
+    _arg(logits, "logits", torch.float32)
+    _arg(bias, "bias", torch.float32, (E,))
+    _arg(topk_ids, "topk_ids", torch.int32, (T, k))
+    _arg(topk_w, "topk_w", torch.float32, (T, k))
+    _gpu(logits=logits, bias=bias, topk_ids=topk_ids, topk_w=topk_w)
     if topk_ids is None:
         topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     if topk_w is None:
@@ -177,8 +203,11 @@ def kmoe_route(logits, bias, k, topk_ids=None, topk_w=None, stream=None):
 
 
 def kmoe_quantize_mx(x, fmt=KMOE_MXFP8_E4M3, codes=None, scales=None, stream=None):
-    _dev(x, "x", torch.bfloat16)
-    rows, cols = x.shape
+    rows, cols = _rows(x, "x", "cols")
+    _arg(x, "x", torch.bfloat16)
+    _arg(codes, "codes", torch.uint8, (rows, cols if fmt == KMOE_MXFP8_E4M3 else cols // 2))
+    _arg(scales, "scales", torch.uint8, (rows, cols // 32))
+    _gpu(x=x, codes=codes, scales=scales)
     if codes is None:
         codes = torch.empty((rows, cols if fmt == KMOE_MXFP8_E4M3 else cols // 2), dtype=torch.uint8,
                             device=x.device)
@@ -196,7 +225,8 @@ def kmoe_prepared_weight_bytes(p, which):
 def kmoe_prepare_weights(p, w13, w13_sf, w2, w2_sf, stream=None):
     """Raw checkpoint tensors -> (w13_k, w2_k) prepared weight blocks."""
     for n, t in (("w13", w13), ("w13_sf", w13_sf), ("w2", w2), ("w2_sf", w2_sf)):
-        _dev(t, n, torch.uint8)
+        _arg(t, n, torch.uint8)
+    _gpu(w13=w13, w13_sf=w13_sf, w2=w2, w2_sf=w2_sf)
     if (w13.numel() != p.E * 2 * p.I * p.H // 2 or w13_sf.numel() != p.E * 2 * p.I * p.H // 32 or
             w2.numel() != p.E * p.H * p.I // 2 or w2_sf.numel() != p.E * p.H * p.I // 32):
         raise ValueError("weight sizes do not match the parameters (w13 [E, 2I, H/2], w2 [E, H, I/2])")
@@ -207,24 +237,33 @@ def kmoe_prepare_weights(p, w13, w13_sf, w2, w2_sf, stream=None):
     return a, b
 
 
+def _layer_args(p, x, w13_k, w2_k, out, workspace=None):
+    """Checks of the arguments every forward entry point shares."""
+    _arg(x, "x", torch.bfloat16, (p.T, p.H))
+    _arg(w13_k, "w13_k", torch.uint8, min_bytes=kmoe_prepared_weight_bytes(p, 0))
+    _arg(w2_k, "w2_k", torch.uint8, min_bytes=kmoe_prepared_weight_bytes(p, 1))
+    _arg(out, "out", torch.bfloat16, (p.T, p.H))
+    _arg(workspace, "workspace", torch.uint8, min_bytes=kmoe_workspace_size(p))
+
+
 def kmoe_forward(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=None, out=None, workspace=None,
                  stream=None, stage_events=None):
     """stage_events: optional list of 7 torch.cuda.Event recorded between the stages (kmoe_forward_ex)."""
-    _dev(x, "x", torch.bfloat16)
-    _dev(w13_k, "w13_k", torch.uint8)
-    _dev(w2_k, "w2_k", torch.uint8)
+    _layer_args(p, x, w13_k, w2_k, out, workspace)
     if topk_ids is None:
-        _dev(logits, "logits", torch.float32)
-        _dev(bias, "bias", torch.float32)
+        _arg(logits, "logits", torch.float32, (p.T, p.E))
+        _arg(bias, "bias", torch.float32, (p.E,))
     else:
-        _dev(topk_ids, "topk_ids", torch.int32)
-        _dev(topk_w, "topk_w", torch.float32)
+        _arg(topk_ids, "topk_ids", torch.int32, (p.T, p.k))
+        _arg(topk_w, "topk_w", torch.float32, (p.T, p.k))
+    _gpu(x=x, logits=logits, bias=bias, w13_k=w13_k, w2_k=w2_k, topk_ids=topk_ids, topk_w=topk_w, out=out,
+         workspace=workspace)
     if out is None:
         out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
         workspace = torch.empty(kmoe_workspace_size(p), dtype=torch.uint8, device=x.device)
     args = (ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13_k), _ptr(w2_k), _ptr(topk_ids),
-            _ptr(topk_w), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+            _ptr(topk_w), _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream))
     if stage_events is None:
         _check("kmoe_forward", _lib.kmoe_forward(*args))
     else:
@@ -241,13 +280,16 @@ def kmoe_router(x, w_gate, bias, k, logits=None, topk_ids=None, topk_w=None, wor
     """The fused router: logits = x @ w_gate^T (bf16 operands, fp32) and the
     top-k routing of kmoe_route, in one kernel.  Returns (topk_ids, topk_w,
     logits, workspace); the workspace's first word is the device error word."""
-    _dev(x, "x", torch.bfloat16)
-    _dev(w_gate, "w_gate", torch.bfloat16)
-    _dev(bias, "bias", torch.float32)
-    T, H = x.shape
-    E = w_gate.shape[0]
-    if w_gate.shape[1] != H:
-        raise ValueError(f"w_gate must be [E, {H}], got {tuple(w_gate.shape)}")
+    T, H = _rows(x, "x", "H")
+    E, _ = _rows(w_gate, "w_gate", "H")
+    _arg(x, "x", torch.bfloat16)
+    _arg(w_gate, "w_gate", torch.bfloat16, (E, H))
+    _arg(bias, "bias", torch.float32, (E,))
+    _arg(logits, "logits", torch.float32, (T, E))
+    _arg(topk_ids, "topk_ids", torch.int32, (T, k))
+    _arg(topk_w, "topk_w", torch.float32, (T, k))
+    _arg(workspace, "workspace", torch.uint8, min_bytes=kmoe_router_workspace_size(T, H, E))
+    _gpu(x=x, w_gate=w_gate, bias=bias, logits=logits, topk_ids=topk_ids, topk_w=topk_w, workspace=workspace)
     dev = x.device
     if logits is None:
         logits = torch.empty((T, E), dtype=torch.float32, device=dev)
@@ -258,7 +300,7 @@ def kmoe_router(x, w_gate, bias, k, logits=None, topk_ids=None, topk_w=None, wor
     if workspace is None:
         workspace = torch.empty(kmoe_router_workspace_size(T, H, E), dtype=torch.uint8, device=dev)
     _check("kmoe_router", _lib.kmoe_router(_ptr(x), _ptr(w_gate), _ptr(bias), T, H, E, k, _ptr(logits),
-                                           _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), workspace.numel(),
+                                           _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), _nbytes(workspace),
                                            _stream(stream)))
     return topk_ids, topk_w, logits, workspace
 
@@ -267,11 +309,10 @@ def kmoe_forward_router(p, x, w_gate, bias, w13_k, w2_k, out=None, workspace=Non
                         stage_events=None):
     """kmoe_forward with the fused router (routing from x and the gate weight
     instead of given logits).  stage_events: optional list of 7 torch.cuda.Event."""
-    _dev(x, "x", torch.bfloat16)
-    _dev(w_gate, "w_gate", torch.bfloat16)
-    _dev(bias, "bias", torch.float32)
-    _dev(w13_k, "w13_k", torch.uint8)
-    _dev(w2_k, "w2_k", torch.uint8)
+    _layer_args(p, x, w13_k, w2_k, out, workspace)
+    _arg(w_gate, "w_gate", torch.bfloat16, (p.E, p.H))
+    _arg(bias, "bias", torch.float32, (p.E,))
+    _gpu(x=x, w_gate=w_gate, bias=bias, w13_k=w13_k, w2_k=w2_k, out=out, workspace=workspace)
     if out is None:
         out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
     if workspace is None:
@@ -279,7 +320,7 @@ def kmoe_forward_router(p, x, w_gate, bias, w13_k, w2_k, out=None, workspace=Non
     ev = None if stage_events is None else kmoe_stage_events(*[e.cuda_event for e in stage_events])
     _check("kmoe_forward_router", _lib.kmoe_forward_router(
         ctypes.byref(p), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(w13_k), _ptr(w2_k), _ptr(out), _ptr(workspace),
-        workspace.numel(), _stream(stream), None if ev is None else ctypes.byref(ev)))
+        _nbytes(workspace), _stream(stream), None if ev is None else ctypes.byref(ev)))
     return out, workspace
 
 
@@ -289,7 +330,16 @@ def kmoe_forward_noalloc(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=
     allocate device memory: the library's built-in scratch array
     (NOALLOC_SCRATCH_BYTES, shared by all calls) is used instead.  `out` and
     the optional `device_error` (one int32 on the device) are caller-owned."""
-    _dev(x, "x", torch.bfloat16)
+    _layer_args(p, x, w13_k, w2_k, out)
+    if topk_ids is None:
+        _arg(logits, "logits", torch.float32, (p.T, p.E))
+        _arg(bias, "bias", torch.float32, (p.E,))
+    else:
+        _arg(topk_ids, "topk_ids", torch.int32, (p.T, p.k))
+        _arg(topk_w, "topk_w", torch.float32, (p.T, p.k))
+    _arg(device_error, "device_error", min_bytes=4)
+    _gpu(x=x, logits=logits, bias=bias, w13_k=w13_k, w2_k=w2_k, topk_ids=topk_ids, topk_w=topk_w, out=out,
+         device_error=device_error)
     if out is None:
         out = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=x.device)
     _check("kmoe_forward_noalloc", _lib.kmoe_forward_noalloc(
@@ -299,6 +349,8 @@ def kmoe_forward_noalloc(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=
 
 
 def kmoe_device_error(workspace, stream=None):
+    _arg(workspace, "workspace", min_bytes=4)
+    _gpu(workspace=workspace)
     word = ctypes.c_uint32(0)
     st = _lib.kmoe_device_error(_ptr(workspace), ctypes.byref(word), _stream(stream))
     return st, word.value
@@ -310,12 +362,16 @@ def kmoe_tile_sf_offset(tile, local_row, g, tile_rows, K, max_tiles):
 
 def kmoe_mma_peak_run(iters, N, workspace, stream=None):
     """Launch the tensor-pipe roof kernel; returns the launch's FLOP count."""
+    _arg(workspace, "workspace", min_bytes=4)
+    _gpu(workspace=workspace)
     _check("kmoe_mma_peak_run", _lib.kmoe_mma_peak_run(iters, N, _ptr(workspace), _stream(stream)))
     sms = torch.cuda.get_device_properties(workspace.device).multi_processor_count
     return sms * iters * 4 * 2 * 128 * N * 32
 
 
 def kmoe_selftest_wait_timeout(workspace, budget_us, stream=None):
+    _arg(workspace, "workspace", min_bytes=4)
+    _gpu(workspace=workspace)
     _check("kmoe_selftest_wait_timeout",
            _lib.kmoe_selftest_wait_timeout(_ptr(workspace), budget_us, _stream(stream)))
 

@@ -108,3 +108,52 @@ def test_weight_generator_numpy_equals_torch():
     per = 2 * big.I * big.H // 32
     words = W._scales_np(W.S_W13SF, 4 * per, 2 * per, big.sf_lo, big.sf_hi, W.SEED)
     assert np.array_equal(sub["w13_sf"][0].ravel(), words[per:])
+
+
+def test_binding_rejects_mis_sized_tensors_before_the_library(K):
+    """The C ABI sees plain pointers; the binding checks every caller tensor's
+    dtype, shape or byte size before a pointer reaches the library (host
+    tensors here: the size checks come before the device check)."""
+    bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+
+    def rejects(fn, needle):
+        with pytest.raises(ValueError, match=needle):
+            fn()
+
+    lg = torch.zeros(4, 8)
+    rejects(lambda: K.kmoe_route(lg, torch.zeros(7), 2), r"bias must have shape \(8,\)")
+    rejects(lambda: K.kmoe_route(lg, torch.zeros(8), 2, topk_ids=torch.zeros(4, 3, dtype=i32)), "topk_ids")
+    rejects(lambda: K.kmoe_route(lg, torch.zeros(8), 2, topk_ids=torch.zeros(4, 2)), "topk_ids must be torch.int32")
+    rejects(lambda: K.kmoe_route(torch.zeros(8), torch.zeros(8), 2), "2-D")
+    rejects(lambda: K.kmoe_route(lg, torch.zeros(8), 2), "CUDA tensor")   # sizes right, host memory
+    x = torch.zeros(4, 128, dtype=bf)
+    rejects(lambda: K.kmoe_quantize_mx(x, codes=torch.zeros(4, 64, dtype=u8)), "codes must have shape")
+    rejects(lambda: K.kmoe_quantize_mx(x, K.KMOE_MXFP4_E2M1, codes=torch.zeros(4, 128, dtype=u8)), "codes")
+    rejects(lambda: K.kmoe_quantize_mx(x, scales=torch.zeros(4, 2, dtype=u8)), "scales")
+
+    p = K.make_params(4, 128, 128, 8, 2)
+    w13 = torch.zeros(K.kmoe_prepared_weight_bytes(p, 0), dtype=u8)
+    w2 = torch.zeros(K.kmoe_prepared_weight_bytes(p, 1), dtype=u8)
+    b = torch.zeros(8)
+    fwd = K.kmoe_forward
+    rejects(lambda: fwd(p, torch.zeros(4, 256, dtype=bf), lg, b, w13, w2), r"x must have shape \(4, 128\)")
+    rejects(lambda: fwd(p, x.float(), lg, b, w13, w2), "x must be torch.bfloat16")
+    rejects(lambda: fwd(p, x, lg, b, w13[:-1], w2), "w13_k holds")
+    rejects(lambda: fwd(p, x, lg, b, w13, w2[:-16]), "w2_k holds")
+    rejects(lambda: fwd(p, x, torch.zeros(4, 9), b, w13, w2), "logits must have shape")
+    rejects(lambda: fwd(p, x, None, None, w13, w2, topk_ids=torch.zeros(4, 3, dtype=i32),
+                        topk_w=torch.zeros(4, 3)), "topk_ids")
+    rejects(lambda: fwd(p, x, lg, b, w13, w2, out=torch.zeros(4, 128)), "out must be torch.bfloat16")
+    rejects(lambda: fwd(p, x, lg, b, w13, w2, workspace=torch.zeros(K.kmoe_workspace_size(p), dtype=f32)),
+            "workspace must be torch.uint8")
+    rejects(lambda: fwd(p, x, lg, b, w13, w2, workspace=torch.zeros(K.kmoe_workspace_size(p) - 1, dtype=u8)),
+            "workspace holds")
+    rejects(lambda: K.kmoe_forward_noalloc(p, x, lg, b, w13, w2, device_error=torch.zeros(0, dtype=i32)),
+            "device_error holds")
+    # the fused router: gate weight [E, H], logits [T, E]
+    wg = torch.zeros(8, 128, dtype=bf)
+    rejects(lambda: K.kmoe_router(x, torch.zeros(8, 64, dtype=bf), b, 2), r"w_gate must have shape \(8, 128\)")
+    rejects(lambda: K.kmoe_router(x, wg, b, 2, logits=torch.zeros(4, 7)), "logits")
+    rejects(lambda: K.kmoe_router(x, wg, b, 2, workspace=torch.zeros(1, dtype=u8)), "workspace holds")
+    rejects(lambda: K.kmoe_forward_router(p, x, torch.zeros(9, 128, dtype=bf), b, w13, w2), "w_gate")
+    rejects(lambda: K.kmoe_device_error(torch.zeros(3, dtype=u8)), "workspace holds")

@@ -54,7 +54,7 @@ def _rank(rank, world, port, out):
 
 def test_two_rank_expert_parallel_sum_equals_the_layer():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
