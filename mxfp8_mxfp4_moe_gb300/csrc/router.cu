@@ -25,7 +25,9 @@
 // The GEMM warps join the routing pool when their work runs out, so routing
 // of finished token tiles overlaps the gate GEMM of the rest.  Every wait is
 // bounded; a wait that gives up sets the timeout bit and the token is left
-// masked (ids -1).
+// masked (ids -1).  When there are enough token tiles (prefill), the plan
+// takes router_pair_kernel instead: the same roles on clusters of two CTAs
+// with M = 256 tensor-core pairs.
 #include "gemm_dev.cuh"  // named_barrier_and
 #include "route_dev.cuh"
 #include "router.cuh"
