@@ -168,7 +168,11 @@ int kmoe_router(const void* x_bf16, const void* w_gate_bf16, const float* bias, 
                 float* logits, int32_t* topk_ids, float* topk_w, void* workspace, size_t ws_bytes,
                 cudaStream_t stream);
 
-/* Microscaling quantisation of bf16 rows, one UE8M0 scale per 32 columns.
+/* Microscaling quantisation of bf16 rows, one UE8M0 scale per 32 columns
+ * (Kimi-K3 MoE path analysis page, SM100 section, mega_moe_pre_dispatch:
+ * bf16 -> per-32 absmax -> UE8M0 scale -> FP8 E4M3 codes, four scale bytes
+ * per int32; the NaN/Inf handling follows the SM120 FlashInfer MXFP4 page's
+ * NaN/Inf decision record: saturating-finite payload, no 0xFF scale byte).
  * Scale byte = e + 127 with e the smallest integer such that
  * amax <= qmax * 2^e (qmax = 448 for E4M3, 6 for E2M1), clamped to
  * [-127, 127]; NaN is ignored by the absmax; codes are round-to-nearest-even
@@ -289,10 +293,13 @@ int kmoe_selftest_wait_timeout(void* workspace, int budget_us, cudaStream_t stre
  * T = 16 at H = 7168, I = 3584, E = 896, k = 16 needs about 21 MiB).  Nothing
  * is allocated or freed.  The first call on a device looks up the array's
  * device address with that device current; make that first call before any
- * stream capture.  Every call uses the same array, which keeps the previous
- * call's contents, so calls that can overlap on the GPU race: order them.
+ * stream capture.  A device reset (cudaDeviceReset) ends the context that
+ * address belongs to; the first call after it looks the address up again.
+ * Every call uses the same array, which keeps the previous call's contents,
+ * so calls that can overlap on the GPU race: order them.
  * device_error (device pointer, optional) receives the call's device error
- * word (the bits kmoe_device_error reports) when the stream reaches it. */
+ * word (the bits kmoe_device_error reports) when the stream reaches it; an
+ * empty batch (T = 0) writes 0 there. */
 int kmoe_forward_noalloc(const kmoe_params* p, const void* x_bf16, const float* logits, const float* bias,
                          const uint8_t* w13_k, const uint8_t* w2_k, const int32_t* topk_ids, const float* topk_w,
                          void* out_bf16, uint32_t* device_error, cudaStream_t stream);

@@ -13,6 +13,16 @@ namespace kmoe {
 constexpr int kRankChunk = 1024;  // slots per block in the stable rank pass
 constexpr int kMaxE = 1024;       // experts supported by the routing kernel
 constexpr int kMaxK = 32;
+constexpr int kMaxDevices = 64;   // devices whose per-device launch state the library keeps
+
+// The current device's ordinal, or -1 if it cannot be read or is not below
+// kMaxDevices (launch state such as a kernel's shared-memory attribute or its
+// co-resident cluster count is kept per device).
+__host__ inline int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
 
 // ---------------------------------------------------------------- tile layout
 // Scales of the B operand (token rows) are stored per token tile so that a

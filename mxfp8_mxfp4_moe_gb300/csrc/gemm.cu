@@ -352,11 +352,13 @@ cudaError_t launch_prep_weights(const uint8_t* codes, const uint8_t* sf, uint8_t
 // ---------------------------------------------------------------- launch
 template <class C>
 static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st) {
-  static bool attr_set = false;  // per instantiation; benign race (idempotent)
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};  // per instantiation and device; benign race (idempotent)
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   moe_gemm_kernel<C><<<grid * C::CTAS_PER_SM, C::THREADS, C::SMEM, st>>>(maps, a);
   return cudaGetLastError();

@@ -368,7 +368,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
 
 template <class C>
 static cudaError_t launch_pair(const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
-  static int pairs = 0;  // co-resident clusters of two (per instantiation; idempotent)
+  static int pairs_of[kMaxDevices] = {};  // co-resident clusters of two (per instantiation and device)
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int& pairs = pairs_of[dev];
   if (pairs == 0) {
     cudaError_t e = cudaFuncSetAttribute(moe_gemm_pair_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);

@@ -58,11 +58,13 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int N, uint
 
 cudaError_t launch_mma_peak(int iters, int N, int grid, uint32_t* err, cudaStream_t st) {
   const int smem = 1024 + 16384 + 32768 + 1536 + 64;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};  // per device (idempotent)
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   mma_peak_kernel<<<grid, 128, smem, st>>>(iters, N, err);
   return cudaGetLastError();

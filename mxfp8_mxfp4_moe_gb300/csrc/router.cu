@@ -538,7 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
 
 template <int KPL>
 cudaError_t launch_pair_kpl(const RouterMaps& maps, const RouterArgs& a, int sms, cudaStream_t st) {
-  static int pairs = 0;  // co-resident clusters of two (per instantiation; idempotent)
+  static int pairs_of[kMaxDevices] = {};  // co-resident clusters of two (per instantiation and device)
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int& pairs = pairs_of[dev];
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -569,7 +572,10 @@ cudaError_t launch_pair_kpl(const RouterMaps& maps, const RouterArgs& a, int sms
 
 template <int KPL>
 cudaError_t launch_kpl(const RouterMaps& maps, const RouterArgs& a, int sms, cudaStream_t st) {
-  static int ready = 0;  // attribute set and occupancy checked (per instantiation; idempotent)
+  static int ready_on[kMaxDevices] = {};  // attribute set and occupancy checked (per instantiation and device)
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int& ready = ready_on[dev];
   if (!ready) {
     cudaError_t e = cudaFuncSetAttribute(router_kernel<KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;

@@ -175,13 +175,12 @@ def forward(w, x_bits, logits, bias, wts, experts_host=None, tokens=None,
               (the expert id of row i of each array), or for all experts
     ids/topk_w  optional precomputed routing (ids < 0 are masked slots)
     Returns dict with out (float64 [n,H]), out_bf16, and stage tensors."""
-    from workloads import bf16_bits_to_f64
     H, I, k = w.H, w.I, w.k
     check_shapes(H, I, wts["w13"], wts["w2"])
     if ids is None:
         ids, topk_w, _ = route(logits, bias, k)
     tokens = np.arange(w.T) if tokens is None else np.asarray(tokens)
-    xq, xs = F.quantize_mx(bf16_bits_to_f64(x_bits[tokens]), "e4m3")
+    xq, xs = F.quantize_mx(F.bf16_decode(x_bits[tokens]), "e4m3")
     sub_ids = ids[tokens]
     sub_w = topk_w[tokens]
     n = len(tokens)

@@ -53,6 +53,31 @@ def test_empty_batch_every_entry_point(K):
     torch.cuda.synchronize()
     assert torch.all(sentinel.float() == 7.0)
 
+    # an empty batch through the no-allocation forward reports its own (empty)
+    # error word, not the one an earlier call left in the shared scratch: the
+    # earlier call routes a slot to expert 99 >= E (error bit 2)
+    import ctypes
+    p1 = params(w, T=1)
+    x1 = torch.zeros((1, w.H), dtype=torch.bfloat16, device=dev)
+    bad_ids = torch.tensor([[1, 99]], dtype=torch.int32, device=dev)
+    bad_w = torch.tensor([[0.5, 0.5]], dtype=torch.float32, device=dev)
+    o1 = torch.empty((1, w.H), dtype=torch.bfloat16, device=dev)
+    err = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    lib = K.lib()
+    cur = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = lib.kmoe_forward_noalloc(ctypes.byref(p1), ctypes.c_void_p(x1.data_ptr()), None, None,
+                                  ctypes.c_void_p(wt["w13_k"].data_ptr()), ctypes.c_void_p(wt["w2_k"].data_ptr()),
+                                  ctypes.c_void_p(bad_ids.data_ptr()), ctypes.c_void_p(bad_w.data_ptr()),
+                                  ctypes.c_void_p(o1.data_ptr()), ctypes.c_void_p(err.data_ptr()), cur)
+    torch.cuda.synchronize()
+    assert st == 0 and (int(err.item()) & 2)
+    err.fill_(-1)
+    st = lib.kmoe_forward_noalloc(ctypes.byref(p0), None, None, None, ctypes.c_void_p(wt["w13_k"].data_ptr()),
+                                  ctypes.c_void_p(wt["w2_k"].data_ptr()), None, None, None,
+                                  ctypes.c_void_p(err.data_ptr()), cur)
+    torch.cuda.synchronize()
+    assert st == 0 and int(err.item()) == 0
+
     # the next non-empty call is unaffected
     out, ws, p, s, _ = run_forward(w)
     tokens = np.arange(w.T)
