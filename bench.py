@@ -38,6 +38,20 @@ METRIC = "Kimi-K3 MoE layer tokens/s & TFLOP/s at T=8192; µs/layer at T=16 (1×
 HEADLINE = "prefill"     # T=8192 layer
 DECODE = "decode"        # T=16 layer
 KERNEL_LAUNCHES_PER_STEP = 7  # route, rank, scan, quantise-scatter, FC1, FC2, combine
+ROUNDS = 5               # interleaved timing rounds (median reported)
+# the five seeded workloads, timed in turn within every round; the small ones
+# (inputs that fit in L2) with the L2 flushed before every timed forward
+INTERLEAVED = ("prefill", "decode", "skewed", "reduced", "tiny")
+FLUSHED = ("reduced", "tiny")
+
+
+def headline_config(world_size: int) -> dict:
+    """The `config` block of the headline line (both arms print the same)."""
+    wp = W.WORKLOADS[HEADLINE]
+    return {"workload": "Kimi-K3 MoE layer prefill chunk T=8192 H=7168 I=3584 E=896 top-16 (SiTU 4/25)",
+            "global_batch": wp.T * world_size, "seq_len": wp.T,
+            "parallelism": "replicas" if world_size > 1 else "single-gpu",
+            "l2": "inputs larger than L2 (36.7 GB of expert weights streamed every step)"}
 
 
 def dist_env():
@@ -158,6 +172,17 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- peaks
+L2_BYTES = 129 << 20  # GB300 L2 (MB as nvidia reports it, rounded up)
+
+WORKLOAD_TEXT = {
+    "tiny": "Tiny MoE layer T=16 H=128 I=128 E=8 top-2",
+    "reduced": "Reduced-expert Kimi-K3 layer T=128 H=7168 I=3584 E=64 top-16",
+    "decode": "Kimi-K3 MoE layer decode T=16 H=7168 I=3584 E=896 top-16",
+    "prefill": "Kimi-K3 MoE layer prefill chunk T=8192 H=7168 I=3584 E=896 top-16",
+    "skewed": "Skewed-routing Kimi-K3 layer T=2048 H=7168 I=3584 E=896 top-16 (Zipf s=1.2 bias, max +3.0)",
+}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -271,6 +296,69 @@ def time_layer(layer, steps, warmup, dist, device, clocks=None):
     barrier(dist)
     total_ms = start.elapsed_time(end)
     return total_ms, clk
+
+
+def time_block(layer, steps):
+    """ms per forward over `steps` back-to-back forwards (CUDA events on the
+    launching stream, synchronised on both sides)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        layer.forward()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def time_flushed(layer, steps, flush):
+    """ms per forward, each forward timed alone right after a write of
+    `flush` (a buffer twice the size of L2), so no input starts in L2."""
+    import torch
+    stream = torch.cuda.current_stream()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        a.record(stream)
+        layer.forward()
+        b.record(stream)
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / steps
+
+
+def time_interleaved(layers, steps, dist, clocks, flush):
+    """ROUNDS rounds; in each, every workload of `layers` is timed in turn
+    (INTERLEAVED order): the headline for about steps / ROUNDS back-to-back
+    forwards (the rounds time exactly `steps` headline forwards), the others
+    for a fixed count.  Returns {name: [ms per forward of each round]} and
+    {name: [forwards in each round]}."""
+    import torch
+    # the headline's `steps` forwards split over the rounds (a round left
+    # with none, when steps < ROUNDS, times the other workloads only)
+    head = [steps // ROUNDS + (1 if r < steps % ROUNDS else 0) for r in range(ROUNDS)]
+    counts = {n: (head if n == HEADLINE else [10 if n in FLUSHED else 20] * ROUNDS) for n in layers}
+    out = {n: [] for n in layers}
+    barrier(dist)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.begin()
+    for r in range(ROUNDS):
+        for n, layer in layers.items():
+            c = counts[n][r]
+            if c == 0:
+                continue
+            out[n].append(time_flushed(layer, c, flush) if n in FLUSHED else time_block(layer, c))
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.end()
+    barrier(dist)
+    return out, counts
 
 
 def time_graph(layer, steps):
@@ -478,12 +566,16 @@ def run_reference(args):
         if i >= args.warmup:
             per_step.append((tps, ntok, secs))
     tps = sum(x[1] for x in per_step) / sum(x[2] for x in per_step)
+    step_ms = 1000.0 * sum(x[2] for x in per_step) / len(per_step)
     line = {
         "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1000.0 * w.T / tps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": "Kimi-K3 MoE layer prefill chunk T=8192 H=7168 I=3584 E=896 top-16",
-                   "global_batch": w.T, "seq_len": w.T, "parallelism": "replicas"},
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; random MXFP4 weights of the Kimi-K3 expert shapes)",
+        "impl": "reference",
+        "config": headline_config(args.gpus),
+        "step": "a bounded sample of the layer per step: random (token, expert slot) pairs until "
+                f"{args.ref_step_s:g} s of oracle time; ms_per_step is that measured time",
+        "ms_per_layer_extrapolated": 1000.0 * w.T / tps,
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{round(sum(x[1] for x in per_step) * w.k)} random (token, expert slot) pairs "
                                    f"over {args.steps} steps = {sum(x[1] for x in per_step):.3g} token equivalents "
@@ -507,46 +599,89 @@ def run_ours(args):
         raise SystemExit(f"kmoe_check_device: {K.kmoe_status_string(st)}")
     peaks, peaks_kind = measured_peaks()
 
-    # ---- headline: T=8192 prefill chunk
+    # ---- the five workloads, timed in interleaved rounds; the headline is T=8192
     wp = W.WORKLOADS[HEADLINE]
     layer = Layer(wp, device)
+    weights = layer.weights
+    layers = {}
+    for n in INTERLEAVED:
+        w_ = W.WORKLOADS[n]
+        if n == HEADLINE:
+            layers[n] = layer
+        elif (w_.E, w_.H, w_.I) == (wp.E, wp.H, wp.I):
+            layers[n] = Layer(w_, device, weights=weights)   # the same 896 experts
+        else:
+            layers[n] = Layer(w_, device)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     clocks = ClockSampler(local) if rank == 0 else None
-    total_ms, clk = time_layer(layer, args.steps, args.warmup, dist, device, clocks)
-    tokens_s, total_ms = job_throughput(dist, ws, wp.T, args.steps, total_ms, device)
-    ms_step = total_ms / args.steps
+    if clocks:
+        clocks.start()  # running well before the timed region begins
+    for L in layers.values():
+        for _ in range(args.warmup):
+            L.forward()
+    torch.cuda.synchronize()
+    for L in layers.values():
+        L.check()
+    rounds, counts = time_interleaved(layers, args.steps, dist, clocks, flush)
+    clk = clocks.stop() if clocks else None
+    for L in layers.values():
+        L.check()
+    med = {n: statistics.median(v) for n, v in rounds.items()}
+    tokens_s, ms_step = job_throughput(dist, ws, wp.T, 1, med[HEADLINE], device)
     tflops = wp.flops() / (ms_step / 1e3) / 1e12
+    # the FP8 peak: 2 x the measured bf16 burst when the SM clock stayed near
+    # its maximum through the timed region, else 2 x the sustained figure
+    sm, sm_max = (clk or {}).get("sm_mhz"), (clk or {}).get("sm_max_mhz")
+    near_max = bool(sm and sm_max and sm >= 0.97 * sm_max)
+    bf16_kind = "bf16_tflops" if near_max else "bf16_tflops_sustained"
+    fp8_peak = 2.0 * peaks[bf16_kind]
+    peak_source = (f"{peaks_kind}: 2 x {bf16_kind} (nominal FP8/BF16 ratio 2); "
+                   f"{'burst' if near_max else 'sustained'} because the median SM clock in the timed region was "
+                   f"{sm} MHz of {sm_max} MHz")
+    configs = {}
+    for n in INTERLEAVED:
+        w_, L, m = W.WORKLOADS[n], layers[n], reduce_max(dist, med[n], device)
+        touched = L.touched_experts()
+        wbytes = touched * w_.expert_weight_bytes()
+        alg = wbytes + 2.0 * w_.T * w_.H * 2 + 4.0 * w_.T * w_.E + 4.0 * w_.E
+        configs[n] = {
+            "workload": WORKLOAD_TEXT[n], "us_per_layer": 1000.0 * m, "tokens_per_s": w_.T / (m / 1e3),
+            "tflops": w_.flops() / (m / 1e3) / 1e12, "fp8_frac": w_.flops() / (m / 1e3) / 1e12 / fp8_peak,
+            "touched_experts": touched, "algorithmic_bytes": alg, "layer_GBs": alg / (m / 1e3) / 1e9,
+            "hbm_frac": alg / (m / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "tile_rows": K.kmoe_workspace_layout(L.p).tile_rows,
+            "rounds_ms": rounds[n], "forwards_per_round": [c for c in counts[n] if c],
+            "timing": ("each forward timed alone after a write of 2 x L2 (inputs fit in L2)" if n in FLUSHED
+                       else "back-to-back forwards (weights larger than L2)")}
+    # kernels of this library launched in the timed region: 7 per forward
+    # (route, rank, scan, quantise-scatter, FC1, FC2, combine), 6 when the
+    # layer has at most 1024 routed slots (the permutation runs in one block)
+    gpu_launches = sum(sum(counts[n]) * (KERNEL_LAUNCHES_PER_STEP if W.WORKLOADS[n].R > 1024
+                                         else KERNEL_LAUNCHES_PER_STEP - 1) for n in layers)
     stages = time_stages(layer, max(3, min(args.steps, 10)))
     layer.check()
     fc1_ms = stages[3]
     fc1_flops = 4.0 * wp.R * wp.H * wp.I
     fc1_tf = fc1_flops / (fc1_ms / 1e3) / 1e12
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
     traffic = fc1_traffic_record()
     e2e_ms, h2d, d2h = e2e_time(layer, args.steps, max(1, args.warmup // 2))
     e2e_tok_s, e2e_ms = job_throughput(dist, ws, wp.T, args.steps, e2e_ms, device)
-    touched_p = layer.touched_experts()
-    weights = layer.weights
-    del layer
-    torch.cuda.empty_cache()
+    touched_p = configs[HEADLINE]["touched_experts"]
 
     # ---- decode: T=16 (same experts, same weights)
     wd = W.WORKLOADS[DECODE]
-    dl = Layer(wd, device, weights=weights)
-    d_total, _ = time_layer(dl, max(args.steps, 20), args.warmup, dist, device, None)
-    d_total = reduce_max(dist, d_total, device)
-    d_us = 1000.0 * d_total / max(args.steps, 20)
+    dl = layers[DECODE]
+    d_us = configs[DECODE]["us_per_layer"]
     d_stages = time_stages(dl, 10)
-    touched = dl.touched_experts()
+    touched = configs[DECODE]["touched_experts"]
     dl.check()
     per_expert_w13 = 2 * wd.I * wd.H // 2 + 2 * wd.I * wd.H // 32
-    per_expert_all = wd.expert_weight_bytes()
     d_fc1_gbs = touched * per_expert_w13 / (d_stages[3] / 1e3) / 1e9
-    d_layer_bytes = touched * per_expert_all + 2 * wd.T * wd.H * 2 + 4 * wd.T * wd.E
-    d_layer_gbs = d_layer_bytes / (d_us / 1e6) / 1e9
-    d_graph_us = time_graph(dl, max(args.steps, 20))
+    d_layer_gbs = configs[DECODE]["layer_GBs"]
+    d_graph_us = time_graph(dl, 20)
     dl.check()
-
-    del dl
+    del dl, layers, flush
+    torch.cuda.empty_cache()
 
     # ---- the SwiGLU control activation on the same prefill layer (same weights)
     wsg = wp.with_(name="prefill_swiglu", activation="swiglu")
@@ -571,7 +706,7 @@ def run_ours(args):
     fr_ms = fr_total / args.steps
     fr_stages = time_stages(rl_, max(3, min(args.steps, 10)))
     rl_.check()
-    del sl, rl_, weights
+    del sl, rl_, weights, layer
     torch.cuda.empty_cache()
     r_pre = time_router(wp, device)
     r_dec = time_router(W.WORKLOADS[DECODE], device)
@@ -616,7 +751,7 @@ def run_ours(args):
         "workload": "Kimi-K3 real checkpoint expert shape H=3584 I=3072 E=896 top-16",
         "prefill_T8192": {"ms_per_layer": r_ms, "tokens_per_s": wr.T / (r_ms / 1e3),
                           "tflops": wr.flops() / (r_ms / 1e3) / 1e12,
-                          "frac_of_fp8_peak": wr.flops() / (r_ms / 1e3) / 1e12 / (2.0 * peaks["bf16_tflops_sustained"]),
+                          "frac_of_fp8_peak": wr.flops() / (r_ms / 1e3) / 1e12 / fp8_peak,
                           "stages_ms": dict(zip(K.STAGE_NAMES, r_stages))},
         "decode_T16": {"us_per_layer": rd_us, "touched_experts": rd_touched,
                        "layer_GBs": rd_bytes / (rd_us / 1e6) / 1e9,
@@ -635,25 +770,28 @@ def run_ours(args):
                          f"before)"}
 
     if rank == 0:
+        cfg = headline_config(ws)
+        cfg.update({"tile_rows": configs[HEADLINE]["tile_rows"], "touched_experts": touched_p,
+                    "timing": f"{ROUNDS} interleaved rounds (each: the five workloads in turn), median; "
+                              f"{[c for c in counts[HEADLINE] if c]} back-to-back T=8192 forwards per round"})
         line = {
             "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "mxfp8xmxfp4 (e4m3 x e2m1, ue8m0 scales, fp32 accumulate, bf16 out)",
             "data": "synthetic (seeded; random MXFP4 weights of the Kimi-K3 expert shapes)",
-            "config": {"workload": "Kimi-K3 MoE layer prefill chunk T=8192 H=7168 I=3584 E=896 top-16 "
-                                   "(SiTU 4/25)", "global_batch": wp.T * ws, "seq_len": wp.T,
-                       "parallelism": "replicas" if ws > 1 else "single-gpu",
-                       "l2": "inputs larger than L2 (36.7 GB of expert weights streamed every step)",
-                       "tile_rows": K.kmoe_workspace_layout(layer_params(K, wp)).tile_rows,
-                       "touched_experts": touched_p},
+            "config": cfg,
             "tflops": tflops,
             "stages_ms": dict(zip(K.STAGE_NAMES, stages)),
             "roofline": {"bound": "tensor", "kernel": "FC1 grouped GEMM (tcgen05 mxf8f6f4, SiTU+requant epilogue)",
                          "achieved": fc1_tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": fc1_tf / fp8_peak,
-                         "peak_source": f"{peaks_kind}: 2 x bf16_tflops_sustained (nominal FP8/BF16 ratio 2)",
+                         "peak_source": peak_source, "sm_mhz_median": sm,
                          "algorithmic": f"4*R*H*I = {fc1_flops:.4g} FLOP per launch",
                          "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
-                         "frac_of_measured_mma_roof": fc1_tf / peak_mma["tflops"]},
+                         "frac_of_measured_mma_roof": fc1_tf / peak_mma["tflops"],
+                         "layer": {"achieved": tflops, "frac": tflops / fp8_peak,
+                                   "frac_of_measured_mma_roof": tflops / peak_mma["tflops"],
+                                   "algorithmic": "6*R*H*I FLOP per layer"}},
+            "configs": configs,
             "mma_peak_measured": peak_mma,
             "real_shape": real_shape,
             "swiglu_control": swiglu_control,
@@ -669,7 +807,7 @@ def run_ours(args):
                                     "algorithmic": f"touched experts x {per_expert_w13} B of w13 codes+scales",
                                     "traffic": None}},
             "e2e": {"value": e2e_tok_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": KERNEL_LAUNCHES_PER_STEP * args.steps,
+            "gpu_launches": gpu_launches,
             "clocks": clk,
             "cpu_baseline": cpu,
             "device": torch.cuda.get_device_name(device),

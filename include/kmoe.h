@@ -277,6 +277,17 @@ int kmoe_mma_peak_run(int iters, int N, void* workspace, cudaStream_t stream);
  * kmoe_device_error, which must then return KMOE_ERR_TIMEOUT). */
 int kmoe_selftest_wait_timeout(void* workspace, int budget_us, cudaStream_t stream);
 
+/* Self-test of the FC1 epilogue's activation: out[i] = the activation that
+ * the forward applies to (gate[i], up[i]), evaluated by the same device
+ * functions in fp32 (SiTU with p->situ_beta and p->situ_linear_beta, or the
+ * SwiGLU control with KMOE_FLAG_SWIGLU and its parameters; SM120 page, SiTU
+ * reference formula and activation table).  It lets a test bound the fp32
+ * evaluation's error against an exact reference.  Only the activation fields
+ * of *p are read (and checked as kmoe_forward checks them); gate, up and out
+ * are device arrays of n floats. */
+int kmoe_selftest_activation(const kmoe_params* p, const float* gate, const float* up, int n, float* out,
+                             cudaStream_t stream);
+
 /* Size of the scratch array built into the library for kmoe_forward_noalloc
  * (32 MiB, reserved on every GPU that loads the library until the process
  * exits). */

@@ -27,7 +27,7 @@ EXPORTS = ("kmoe_status_string", "kmoe_check_device", "kmoe_workspace_size", "km
            "kmoe_route", "kmoe_quantize_mx", "kmoe_prepared_weight_bytes", "kmoe_prepare_weights",
            "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error", "kmoe_tile_sf_offset",
            "kmoe_selftest_wait_timeout", "kmoe_forward_noalloc", "kmoe_mma_peak_run",
-           "kmoe_router_workspace_size", "kmoe_router", "kmoe_forward_router")
+           "kmoe_router_workspace_size", "kmoe_router", "kmoe_forward_router", "kmoe_selftest_activation")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -93,9 +93,10 @@ def load_library(path: str = LIB_PATH):
     lib.kmoe_router_workspace_size.argtypes = [I, I, I]
     lib.kmoe_router.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, V]
     lib.kmoe_forward_router.argtypes = [pp, P, P, P, P, P, P, P, S, V, ctypes.POINTER(kmoe_stage_events)]
+    lib.kmoe_selftest_activation.argtypes = [pp, P, P, I, P, V]
     for n in ("kmoe_check_device", "kmoe_workspace_layout", "kmoe_route", "kmoe_quantize_mx",
               "kmoe_prepare_weights", "kmoe_forward", "kmoe_forward_ex", "kmoe_device_error",
-              "kmoe_selftest_wait_timeout", "kmoe_router", "kmoe_forward_router"):
+              "kmoe_selftest_wait_timeout", "kmoe_router", "kmoe_forward_router", "kmoe_selftest_activation"):
         getattr(lib, n).restype = ctypes.c_int
     return lib
 
@@ -345,6 +346,20 @@ def kmoe_forward_noalloc(p, x, logits, bias, w13_k, w2_k, topk_ids=None, topk_w=
     _check("kmoe_forward_noalloc", _lib.kmoe_forward_noalloc(
         ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13_k), _ptr(w2_k), _ptr(topk_ids), _ptr(topk_w),
         _ptr(out), _ptr(device_error), _stream(stream)))
+    return out
+
+
+def kmoe_selftest_activation(p, gate, up, out=None, stream=None):
+    """The FC1 epilogue's activation of (gate, up), elementwise (fp32 device
+    arrays of one shape), by the forward's own device functions."""
+    _arg(gate, "gate", torch.float32, tuple(gate.shape))
+    _arg(up, "up", torch.float32, tuple(gate.shape))
+    if out is None:
+        out = torch.empty_like(gate)
+    _arg(out, "out", torch.float32, tuple(gate.shape))
+    _gpu(gate=gate, up=up, out=out)
+    _check("kmoe_selftest_activation", _lib.kmoe_selftest_activation(
+        ctypes.byref(p), _ptr(gate), _ptr(up), gate.numel(), _ptr(out), _stream(stream)))
     return out
 
 

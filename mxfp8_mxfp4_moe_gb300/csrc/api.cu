@@ -22,6 +22,8 @@ cudaError_t launch_quant_scatter(const void*, int, int, int, int, int, int, int,
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int, int, int, int, float, void*,
                            cudaStream_t);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t budget_ns, cudaStream_t st);
+cudaError_t launch_activation_selftest(const float*, const float*, int, int, float, float, float, float, float, float,
+                                       float*, cudaStream_t);
 cudaError_t launch_mma_peak(int iters, int N, int grid, uint32_t* err, cudaStream_t st);
 __global__ void kmoe_probe_kernel();
 }  // namespace kmoe
@@ -448,6 +450,25 @@ int kmoe_selftest_wait_timeout(void* workspace, int budget_us, cudaStream_t stre
   if (!workspace || budget_us <= 0 || budget_us > 1000000) return KMOE_ERR_ARG;
   KMOE_CK(launch_wait_selftest(static_cast<uint32_t*>(workspace), static_cast<uint64_t>(budget_us) * 1000ull,
                                stream));
+  return KMOE_OK;
+}
+
+int kmoe_selftest_activation(const kmoe_params* p, const float* gate, const float* up, int n, float* out,
+                             cudaStream_t stream) {
+  if (!p) return KMOE_ERR_ARG;
+  kmoe_params q = *p;  // only the activation fields matter here
+  q.T = 0;
+  q.H = q.I = 128;
+  q.E = q.k = 1;
+  const int st = check_params(&q);
+  if (st != KMOE_OK) return st;
+  if (n < 0) return KMOE_ERR_ARG;
+  if (n > 0 && (!gate || !up || !out)) return KMOE_ERR_ARG;
+  const bool swiglu = (p->flags & KMOE_FLAG_SWIGLU) != 0u;
+  KMOE_CK(launch_activation_selftest(gate, up, n, swiglu ? 1 : 0, static_cast<float>(2.0 / p->situ_beta),
+                                     static_cast<float>(2.0 / p->situ_linear_beta),
+                                     static_cast<float>(static_cast<double>(p->situ_beta) * p->situ_linear_beta),
+                                     p->swiglu_alpha, p->swiglu_beta, p->swiglu_limit, out, stream));
   return KMOE_OK;
 }
 

@@ -199,6 +199,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Work& wk
         const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(act[4 * k4 + 2] * inv, act[4 * k4 + 3] * inv),
                                                      __NV_SATFINITE, __NV_E4M3);
         w[k4] = (lo & 0xFFFFu) | (hi << 16);
+        // a NaN activation (from an accumulator that overflowed to +Inf and
+        // -Inf, possible only for inputs near the bf16 maximum) becomes +0,
+        // the MXFP8 rule for NaN elements: the E4M3 NaN codes 0x7F / 0xFF
+        w[k4] &= ~__vcmpeq4(w[k4] & 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       }
       if (col < wk.n) {
         uint8_t* dst = a.iq + static_cast<size_t>(wk.r0 + col) * a.I + 64 * mt + i0;

@@ -73,6 +73,88 @@ def oracle_forward(w, s, tokens, ids=None, topk_w=None):
                      topk_w=topk_w, want_stages=True)
 
 
+def _oracle_slots_worker(args):
+    """One worker of oracle_forward_pool: the oracle's forward of `tokens`
+    with every slot whose expert is not in `experts` masked (-1), so the
+    stage tensors of the slots it owns come out exactly as in one whole call."""
+    w, x_bits, ids, topk_w, experts = args
+    wts = W.gen_expert_weights_np(w, experts)
+    own = np.isin(ids, experts)
+    masked = np.where(own, ids, -1).astype(np.int32)
+    n = len(ids)
+    r = O.forward(w.with_(T=n), x_bits, None, None, wts, experts_host=list(experts), tokens=np.arange(n),
+                  ids=masked, topk_w=topk_w, want_stages=True)
+    return own, r["inter_q"], r["inter_s"], r["y"]
+
+
+def oracle_forward_pool(w, s, tokens, ids=None, topk_w=None, workers=None):
+    """oracle_forward for many tokens of a full-size layer, with the experts
+    spread over worker processes (started with spawn, so they hold no CUDA
+    state).  Every (token, slot) is computed by one oracle call that owns its
+    expert; the per-slot y are then summed by the oracle's own combine."""
+    import multiprocessing as mp
+    import os
+    if ids is None:
+        ids, topk_w, _ = O.route(s["logits"], s["bias"], w.k)
+    tokens = np.asarray(tokens)
+    sub_ids, sub_w = ids[tokens], topk_w[tokens]
+    used = sorted(set(int(e) for e in sub_ids.ravel() if e >= 0))
+    n_workers = workers or max(1, min(8, (os.cpu_count() or 2) // 2, len(used)))
+    chunks = [used[i::n_workers] for i in range(n_workers)]
+    x_bits = s["x"][tokens]
+    jobs = [(w, x_bits, sub_ids, sub_w, c) for c in chunks if c]
+    old = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for v in old:
+        os.environ[v] = "2"
+    try:
+        with mp.get_context("spawn").Pool(len(jobs)) as pool:
+            parts = pool.map(_oracle_slots_worker, jobs)
+    finally:
+        for v, val in old.items():
+            if val is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = val
+    n, k = sub_ids.shape
+    iq = np.zeros((n, k, w.I), np.uint8)
+    isf = np.zeros((n, k, w.I // 32), np.uint8)
+    y = np.zeros((n, k, w.H), np.float64)
+    for own, q, sf, yy in parts:
+        iq[own], isf[own], y[own] = q[own], sf[own], yy[own]
+    out = O.combine(y, sub_ids, sub_w, w.routed_scaling_factor)
+    return {"out": out, "inter_q": iq, "inter_s": isf, "y": y, "ids": ids, "topk_w": topk_w}
+
+
+def tile_position_tokens(ids: np.ndarray, E: int, BN: int, n: int = 32, seed: int = 0):
+    """Tokens chosen by where their rows land in the expert-sorted token
+    tiles of BN rows (rows of an expert in slot order, as the permutation
+    lays them out): for the three most- and three least-loaded experts and
+    the last expert with rows (whose work items are claimed last), the first
+    row, the rows on both sides of the first tile boundary, a middle row and
+    the last row (the partial tile); then random tokens up to n."""
+    T, k = ids.shape
+    flat = ids.ravel()
+    valid = flat >= 0
+    counts = np.bincount(flat[valid], minlength=E)
+    order = np.flatnonzero(valid)[np.argsort(flat[valid], kind="stable")]
+    starts = np.concatenate([[0], np.cumsum(counts)])
+    nz = np.flatnonzero(counts)
+    by_load = nz[np.argsort(-counts[nz], kind="stable")]
+    chosen = list(dict.fromkeys(list(by_load[:3]) + list(by_load[-3:]) + [nz[-1]]))
+    toks = set()
+    for e in chosen:
+        c = int(counts[e])
+        nt = (c + BN - 1) // BN
+        mid = (nt // 2) * BN + (min(BN, c - (nt // 2) * BN) // 2)
+        rows = {0, mid, c - 1} | ({BN - 1, BN} if nt > 1 else set())
+        for r in rows:
+            toks.add(int(order[starts[e] + r] // k))
+    rng = np.random.default_rng(seed)
+    while len(toks) < min(n, T):
+        toks.add(int(rng.integers(T)))
+    return np.array(sorted(toks)), [int(e) for e in chosen]
+
+
 def output_errors(gpu_bf16: torch.Tensor, ref: np.ndarray):
     g = gpu_bf16.float().cpu().numpy().astype(np.float64)
     diff = g - ref

@@ -12,7 +12,8 @@ import workloads as W
 from oracle import formats as F
 from oracle import moe as O
 from tests._moe_setup import (assert_output_parity, device_inputs, device_weights, gather_row_scales,
-                              oracle_forward, params, run_forward, stage_numpy)
+                              oracle_forward, oracle_forward_pool, params, run_forward, stage_numpy,
+                              tile_position_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,17 +65,47 @@ def _check_stages(w, p, ws, s, ref, tokens):
     assert np.array_equal(st["xq"][rows], xq_ref[slots // w.k])
     got_sf = gather_row_scales(st["xsf"], st, rows, w.H)
     assert np.array_equal(got_sf, xs_ref[slots // w.k])
-    # intermediate codes of the sampled tokens: agreement rate (fp32 vs double SiTU may cross midpoints)
+    # intermediate codes of the sampled tokens (masked slots excluded)
     tsl = np.array([t * w.k + j for t in tokens for j in range(w.k)])
+    tsl = tsl[ids_ref.ravel()[tsl] >= 0]
     iq_gpu = st["iq"][ros[tsl]]
-    iq_ref = ref["inter_q"].reshape(-1, w.I)
-    same = (iq_gpu == iq_ref) | (((iq_gpu | iq_ref) & 0x7F) == 0)
-    rate = same.mean()
+    iq_ref = ref["inter_q"].reshape(-1, w.I)[ids_ref[tokens].ravel() >= 0]
     isf_gpu = gather_row_scales(st["isf"], st, ros[tsl], w.I)
-    sf_rate = (isf_gpu == ref["inter_s"].reshape(-1, w.I // 32)).mean()
-    print(f"{w.name}: intermediate code agreement {rate:.6f}, scale agreement {sf_rate:.6f}")
-    assert rate >= 0.999 and sf_rate >= 0.999
+    isf_ref = ref["inter_s"].reshape(-1, w.I // 32)[ids_ref[tokens].ravel() >= 0]
+    check_intermediate_agreement(w.name, iq_gpu, iq_ref, isf_gpu, isf_ref)
     return st
+
+
+def _e4m3_ordinal(c):
+    """Position of E4M3 codes on the number line (+0 and -0 both 0; codes
+    are monotonic in magnitude within a sign)."""
+    c = c.astype(np.int64)
+    return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+
+
+def check_intermediate_agreement(name, iq_gpu, iq_ref, isf_gpu, isf_ref):
+    """The GPU evaluates the activation in fp32, the oracle in double, so an
+    activation within rounding of an E4M3 midpoint (or a group maximum within
+    rounding of a power-of-two boundary) can quantise one step apart.  Bar:
+    at least 99.99 % of scales and of codes agree (at most one disagreement
+    in samples of fewer than 10^4), every differing scale is one step apart,
+    and every differing code (in groups whose scales agree) is one E4M3 step
+    apart.  No NaN code and no 0xFF scale anywhere."""
+    assert not np.any((iq_gpu & 0x7F) == 0x7F), "NaN intermediate code"
+    assert not np.any(isf_gpu == 0xFF), "0xFF intermediate scale"
+    sf_bad = isf_gpu != isf_ref
+    n_sf = sf_bad.size
+    assert sf_bad.sum() <= max(1, int(1e-4 * n_sf)), f"{name}: {sf_bad.sum()} of {n_sf} scales differ"
+    assert np.all(np.abs(isf_gpu[sf_bad].astype(int) - isf_ref[sf_bad].astype(int)) == 1)
+    group_ok = np.repeat(~sf_bad, 32, axis=1)
+    d = np.abs(_e4m3_ordinal(iq_gpu) - _e4m3_ordinal(iq_ref))[group_ok]
+    n = d.size
+    flips = int((d != 0).sum())
+    rate = 1.0 - flips / max(n, 1)
+    print(f"{name}: intermediate code agreement {rate:.7f} ({flips} of {n} differ), "
+          f"scale agreement {1.0 - sf_bad.mean():.7f}")
+    assert flips <= max(1, int(1e-4 * n)), f"{name}: {flips} of {n} intermediate codes differ"
+    assert np.all(d <= 1), f"{name}: intermediate codes differ by more than one E4M3 step"
 
 
 @pytest.mark.parametrize("wl", [W.WORKLOADS["tiny"], TINY_UNSAT, TINY_BETA, TINY_SWIGLU, TINY_SWIGLU_UNSAT, TINY_SWIGLU_P],
@@ -99,17 +130,26 @@ def test_forward_pair_tiles_every_token(K, wl):
     assert_output_parity(out, ref["out"], wl.name)
 
 
-@pytest.mark.parametrize("name,sample", [("reduced", 6), ("decode", 3), ("prefill", 2), ("skewed", 2)])
-def test_forward_full_size_sampled(K, name, sample):
+@pytest.mark.parametrize("name", ["reduced", "decode", "prefill", "skewed"])
+def test_forward_full_size_tile_positions(K, name):
+    """Full-size layers, outputs and intermediate codes checked on at least
+    32 tokens (all 16 at decode) chosen by tile position: the first row, both
+    sides of the first tile boundary, a middle row and the last (partial-tile)
+    row of the three most- and three least-loaded experts and of the last
+    expert with rows (its work items are claimed last), plus random tokens.
+    Routing, x codes/scales and the permutation are checked on every token."""
     w = W.WORKLOADS[name]
     out, ws, p, s, _ = run_forward(w)
-    rng = np.random.default_rng(123)
-    tokens = np.sort(rng.choice(w.T, size=sample, replace=False))
-    ref = oracle_forward(w, s, tokens)
+    ids, tw, _ = O.route(s["logits"], s["bias"], w.k)
+    BN = K.kmoe_workspace_layout(p).tile_rows
+    tokens, experts = tile_position_tokens(ids, w.E, BN, n=32, seed=123)
+    counts = np.bincount(ids.ravel(), minlength=w.E)
+    print(f"{name}: {len(tokens)} tokens, tile rows {BN}, experts {experts} with rows {counts[experts].tolist()}")
+    assert len(tokens) >= min(32, w.T)
+    ref = oracle_forward_pool(w, s, tokens, ids, tw)
     _check_stages(w, p, ws, s, ref, tokens)
     assert_output_parity(out[torch.from_numpy(tokens).cuda()], ref["out"], name)
-    o = out.float()
-    assert torch.isfinite(o).all()
+    assert torch.isfinite(out.float()).all()
 
 
 @pytest.mark.parametrize("name,sample", [("real_decode", 3), ("real_prefill", 2)])
@@ -162,12 +202,18 @@ def test_forward_expert_parallel_local_slice(K):
     assert_output_parity(out[torch.from_numpy(tokens).cuda()], ref["out"], "ep_local")
 
 
-def test_determinism_and_graph_replay(K):
-    for name in ("tiny", "reduced"):
-        w = W.WORKLOADS[name]
+@pytest.mark.parametrize("name", ["tiny", "reduced", "pair_tiles", "prefill"])
+def test_determinism_and_graph_replay(K, name):
+    """Three eager runs bitwise equal; a CUDA graph captured once and replayed
+    twice bitwise equal to them.  pair_tiles and prefill run the CTA-pair
+    GEMMs, whose FC1 work items are claimed dynamically (the order differs
+    from run to run, the result may not)."""
+    for w in [{"pair_tiles": PAIR_EVEN}.get(name) or W.WORKLOADS[name]]:
         wt = device_weights(w)
         inp, s = device_inputs(w)
         p = params(w)
+        if name in ("pair_tiles", "prefill"):
+            assert K.kmoe_workspace_layout(p).tile_rows == 224
         ws = torch.empty(K.kmoe_workspace_size(p), dtype=torch.uint8, device="cuda")
         outs = []
         for _ in range(3):

@@ -140,3 +140,55 @@ def test_mma_peak_kernel_runs(K):
     assert flops == torch.cuda.get_device_properties(0).multi_processor_count * 2000 * 4 * 2 * 128 * 224 * 32
     with pytest.raises(K.KmoeError):
         K.kmoe_mma_peak_run(10, 200, ws)   # N not a multiple of 16
+
+
+# ---------------------------------------------------------------- the FC1 activation's error
+# The FC1 epilogue evaluates SiTU (and the SwiGLU control) in fp32 from fast
+# exponentials; the oracle evaluates the formula in double.  The relative
+# error bound asserted here is what keeps intermediate-code flips rare: a
+# value flips to the neighbouring E4M3 code only if it lies within that
+# relative distance of a rounding midpoint (midpoints sit 2^-4 .. 2^-3 apart
+# in relative terms), so a bound of 2^-18 allows flips on about 2^-18 * 2^4 =
+# 6e-5 of the values at most.
+ACT_REL_BOUND = 2.0 ** -18
+
+
+def _activation_inputs():
+    rng = np.random.default_rng(11)
+    parts = [rng.normal(0, 108, (2, 400000)), rng.normal(0, 14.5, (2, 400000)), rng.uniform(-40, 40, (2, 400000)),
+             rng.uniform(-1, 1, (2, 200000)), rng.uniform(-1e-3, 1e-3, (2, 100000)),
+             np.array([[0.0, -0.0, 1e-30, 4.0, -4.0, 25.0, -25.0, 88.0, -88.0, 1e30, -1e30, np.inf, -np.inf],
+                       [3.0, 3.0, 1e-30, 25.0, 25.0, -4.0, 4.0, 1.0, 1.0, 1e30, 1.0, 2.0, np.inf]])]
+    gu = np.concatenate(parts, axis=1).astype(np.float32)
+    return gu[0], gu[1]
+
+
+@pytest.mark.parametrize("act,params", [("situ", dict(situ_beta=4.0, situ_linear_beta=25.0)),
+                                        ("situ", dict(situ_beta=2.0, situ_linear_beta=10.0)),
+                                        ("swiglu", dict(swiglu_alpha=1.702, swiglu_beta=1.0, swiglu_limit=7.0))],
+                         ids=["situ_4_25", "situ_2_10", "swiglu"])
+def test_activation_error_bound(K, act, params):
+    g, u = _activation_inputs()
+    if act == "swiglu":
+        # -Inf * sigmoid(-Inf) has no value (the forward maps such a NaN
+        # activation to +0 when it requantises); finite inputs only here
+        keep = np.isfinite(g) & np.isfinite(u)
+        g, u = g[keep], u[keep]
+    p = K.make_params(0, 128, 128, 1, 1, activation=act, **params)
+    out = K.kmoe_selftest_activation(p, torch.from_numpy(g).cuda(), torch.from_numpy(u).cuda()).cpu().numpy()
+    gd, ud = g.astype(np.float64), u.astype(np.float64)
+    if act == "situ":
+        ref = O.situ(gd, ud, params["situ_beta"], params["situ_linear_beta"])
+    else:
+        ref = O.swiglu(gd, ud, params["swiglu_alpha"], params["swiglu_beta"], params["swiglu_limit"])
+    assert np.all(np.isfinite(out))
+    big = np.abs(ref) > 1e-30
+    rel = np.abs(out[big].astype(np.float64) - ref[big]) / np.abs(ref[big])
+    tiny_abs = np.abs(out[~big].astype(np.float64) - ref[~big]).max(initial=0.0)
+    print(f"{act} {params}: max relative error {rel.max():.3e} (= {rel.max() / 2 ** -24:.1f} x 2^-24), "
+          f"mean {rel.mean():.3e}; |ref| <= 1e-30: max abs error {tiny_abs:.1e}")
+    assert rel.max() <= ACT_REL_BOUND
+    assert tiny_abs <= 1e-30
+    # exact zeros stay zero (SiTU(0, u) = SiTU(g, 0) = 0)
+    if act == "situ":
+        assert out[0] == 0.0 and out[1] == 0.0
