@@ -41,9 +41,18 @@
 
 namespace kmoe {
 
-template <int BN_, int KPS_, int STAGES_, bool FC1_, int EPI_WARPS_ = 8, int CTAS_PER_SM_ = 1, int NT_ = 1>
+// Weight stages fetched into L2 ahead of their TMA loads by the small-tile
+// (decode) kernels, which are bound by HBM: the shared-memory ring alone keeps
+// too few weight bytes in flight per SM to cover the memory latency.
+#ifndef KMOE_DECODE_PF_STAGES
+#define KMOE_DECODE_PF_STAGES 2
+#endif
+
+template <int BN_, int KPS_, int STAGES_, bool FC1_, int EPI_WARPS_ = 8, int CTAS_PER_SM_ = 1, int NT_ = 1,
+          int PF_ = 0>
 struct GemmCfg {
   static constexpr int BN = BN_;
+  static constexpr int PF = PF_;          // stages of weights prefetched into L2 ahead of the loads (0: none)
   static constexpr int KPS = KPS_;        // 128-wide K blocks per pipeline stage
   static constexpr int STAGES = STAGES_;
   static constexpr bool FC1 = FC1_;
@@ -134,6 +143,12 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
       const uint64_t pol = is_a ? policy_evict_normal() : policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
+      // L2 prefetch cursor (weight producer, PF > 0): walks the same item and
+      // K-block sequence as the loads, up to PF stages ahead of them
+      int pw = blockIdx.x, pkb = 0;
+      uint32_t pit = 0;
+      Work pwk;
+      if (C::PF > 0 && is_a && pw < total) decode_work(a, tsm, C::BN, C::NT, pw, pwk);
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Work wk;
         decode_work(a, tsm, C::BN, C::NT, w, wk);
@@ -144,6 +159,24 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
         for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
+          if (C::PF > 0 && is_a) {
+            while (pw < total && pit <= it + C::PF) {
+              const int pblk0 = (pwk.e * a.MT + C::NT * pwk.m) * a.KB + pkb;
+#pragma unroll
+              for (int j = 0; j < C::NT; ++j) {
+                const size_t blk = static_cast<size_t>(pblk0 + j * a.KB);
+                bulk_prefetch_l2(a.wq + blk * 8192, C::KPS * 8192);
+                bulk_prefetch_l2(a.wsf + blk * 512, C::KPS * 512);
+              }
+              ++pit;
+              pkb += C::KPS;
+              if (pkb >= a.KB) {
+                pkb = 0;
+                pw += gridDim.x;
+                if (pw < total) decode_work(a, tsm, C::BN, C::NT, pw, pwk);
+              }
+            }
+          }
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
             ok = false;
             break;
@@ -190,10 +223,11 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Lean issue loop (the tensor pipe takes the next MMA only about as fast
-    // as it runs one): descriptors are formed once and advanced by adds (the
-    // start-address field holds smem offset >> 4).
-    if (lane == 0) {
+    // The whole warp runs this loop converged and one elected lane issues each
+    // tcgen05 operation (ptx.cuh, the _el forms); the loop stays lean:
+    // descriptors are formed once and advanced by adds (the start-address
+    // field holds smem offset >> 4).
+    {
       constexpr uint32_t kStageD = C::STAGE >> 4;
       const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
       const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + C::B_OFF));
@@ -207,16 +241,14 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
         decode_work(a, tsm, C::BN, C::NT, w, wk);
         const uint32_t acc = li % C::NACC;
         const uint32_t aph = (li / C::NACC) & 1u;
-        if (!mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
+        if (!mbar_wait_warp(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * C::NT * C::BN;  // tile j accumulates at d + j*BN
         const uint32_t nmma = (static_cast<uint32_t>(wk.n) + 15u) & ~15u;
         const int nch = static_cast<int>((nmma + 127u) >> 7);
-        uint32_t idk[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) idk[kk] = idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, kk, kk);
+        const uint32_t id0 = idesc_mxf8f6f4(128, nmma, MX_E2M1, MX_E4M3, 0, 0);
         for (int kb = 0; kb < a.KB; kb += C::KPS) {
-          if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&full[s], ph, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
@@ -228,30 +260,31 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
             const uint32_t sfc = sf0 + kbi * C::SFW;
             const uint32_t sfb = sfc + 4 * C::NT;
 #pragma unroll
-            for (int j = 0; j < C::NT; ++j) tc_cp_32x128b_warpx4(sfc + 4 * j, sfadesc0 + so + (j * C::KPS + kbi) * 32);
-            tc_cp_32x128b_warpx4(sfb, sfbdesc0 + so + kbi * C::NCH * 32);
-            if (C::NCH > 1 && nch > 1) tc_cp_32x128b_warpx4(sfb + 4, sfbdesc0 + so + kbi * C::NCH * 32 + 32);
+            for (int j = 0; j < C::NT; ++j)
+              tc_cp_32x128b_warpx4_el(sfc + 4 * j, sfadesc0 + so + (j * C::KPS + kbi) * 32);
+            tc_cp_32x128b_warpx4_el(sfb, sfbdesc0 + so + kbi * C::NCH * 32);
+            if (C::NCH > 1 && nch > 1) tc_cp_32x128b_warpx4_el(sfb + 4, sfbdesc0 + so + kbi * C::NCH * 32 + 32);
             const uint64_t bd = bdesc0 + so + kbi * (C::B_KB >> 4);
 #pragma unroll
             for (int j = 0; j < C::NT; ++j) {
               const uint64_t ad = adesc0 + so + (j * C::KPS + kbi) * (C::A_KB >> 4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_mxf8f6f4(d + j * C::BN, ad + 2 * kk, bd + 2 * kk, idk[kk], sfc + 4 * j, sfb,
-                             (kb | kbi | kk) != 0);
+              mma_mxf8f6f4_el(d + j * C::BN, ad, bd, id0, sfc + 4 * j, sfb, (kb | kbi) != 0);
+              mma_mxf8f6f4_el(d + j * C::BN, ad + 2, bd + 2, id0 | (1u << 4) | (1u << 29), sfc + 4 * j, sfb, 1u);
+              mma_mxf8f6f4_el(d + j * C::BN, ad + 4, bd + 4, id0 | (2u << 4) | (2u << 29), sfc + 4 * j, sfb, 1u);
+              mma_mxf8f6f4_el(d + j * C::BN, ad + 6, bd + 6, id0 | (3u << 4) | (3u << 29), sfc + 4 * j, sfb, 1u);
             }
           }
-          tc_commit(&empty[s]);
+          tc_commit_el(&empty[s]);
           if (++s == C::STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&acc_full[acc]);
+        tc_commit_el(&acc_full[acc]);
       }
-      tc_commit(done);
-      mbar_wait_bounded(done, 0, budget, a.err, nullptr);
+      tc_commit_el(done);
+      mbar_wait_warp(done, 0, budget, a.err, nullptr);
     }
   } else if (warp < C::PRODB_WARP) {
     // ------------------------------------------------------------ epilogue
@@ -367,19 +400,20 @@ static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& a, int grid,
 cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, const GemmArgs& a, int grid,
                             cudaStream_t st) {
   if (a.KB % kps != 0) return cudaErrorInvalidValue;
+  constexpr int PF = KMOE_DECODE_PF_STAGES;
   if (fc1) {
-    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, true, 4, 2>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<32, 1, 8, true>>(maps, a, grid, st);
-    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 3, true>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<64, 1, 6, true>>(maps, a, grid, st);
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, true, 4, 2, 1, PF>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<32, 1, 8, true, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
+    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 3, true, 8, 1, 1, PF>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<64, 1, 6, true, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
     if (BN == 224 && kps == 1)
       return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(true, maps, a, grid, st)
                            : launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
   } else {
-    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<32, 1, 8, false>>(maps, a, grid, st);
-    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 4, false>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<64, 1, 7, false>>(maps, a, grid, st);
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2, 1, PF>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<32, 1, 8, false, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
+    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 4, false, 8, 1, 1, PF>>(maps, a, grid, st)
+                                  : launch_one<GemmCfg<64, 1, 7, false, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
     if (BN == 224 && kps == 1)
       return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(false, maps, a, grid, st)
                            : launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st);

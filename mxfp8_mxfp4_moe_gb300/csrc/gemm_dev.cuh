@@ -53,10 +53,36 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads
   return out != 0;
 }
 
-// 1 - exp(-x) and exp(-x) for x >= 0: a Taylor polynomial below 1/4 (no
-// cancellation; truncation error x^8/8! < 4e-10 relative), 1 - q above.
-__device__ __forceinline__ void one_minus_exp_neg(float x, float& om, float& q) {
-  q = __expf(-x);
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// e^(-y) for y >= 0, accurate to a few ulp over the whole range.  The fast
+// form 2^(-fl(y log2 e)) loses accuracy as y grows: the product's rounding is
+// up to |y log2 e| 2^-24 in absolute terms, which becomes the result's
+// relative error.  Here y log2 e is carried as t + tl (tl: the product's
+// rounding residual from an fma plus y times the tail of log2 e), 2^(-t) is
+// taken on the hardware's base-2 exponential and multiplied by
+// 2^(-tl) = 1 - tl ln 2 (|tl| <= 2^-23 |t|).  y is clamped to 128 (e^-128 is
+// below the smallest subnormal; results below 2^-126 flush to zero), so
+// +Inf gives 0 (and so does NaN).
+__device__ __forceinline__ float exp_neg(float y) {
+  constexpr float kLog2e = 1.44269502162933349609375f;  // fp32(log2 e)
+  constexpr float kLog2eLo = 1.925963033500011e-08f;   // fp32(log2 e - kLog2e)
+  constexpr float kLn2 = 0.693147182464599609375f;     // fp32(ln 2)
+  y = fminf(y, 128.0f);
+  const float t = y * kLog2e;
+  const float tl = fmaf(y, kLog2eLo, fmaf(y, kLog2e, -t));
+  const float p = ex2_approx(-t);
+  return fmaf(p, -tl * kLn2, p);
+}
+
+// 1 - exp(-x) for x >= 0 given q = exp(-x): a Taylor polynomial below 1/4
+// (no cancellation; the first omitted term, x^7/8!, is below 2e-9 relative),
+// 1 - q above.
+__device__ __forceinline__ float one_minus_exp_neg(float x, float q) {
   float p = 1.0f / 5040.0f;
   p = fmaf(p, x, -1.0f / 720.0f);
   p = fmaf(p, x, 1.0f / 120.0f);
@@ -64,7 +90,7 @@ __device__ __forceinline__ void one_minus_exp_neg(float x, float& om, float& q) 
   p = fmaf(p, x, 1.0f / 6.0f);
   p = fmaf(p, x, -0.5f);
   p = fmaf(p, x, 1.0f);
-  om = x < 0.25f ? x * p : 1.0f - q;
+  return x < 0.25f ? x * p : 1.0f - q;
 }
 
 // SiTU(g, u) = beta*tanh(g/beta)*sigmoid(g) * beta_lin*tanh(u/beta_lin) in fp32
@@ -72,13 +98,24 @@ __device__ __forceinline__ void one_minus_exp_neg(float x, float& om, float& q) 
 //   tanh(|v|/b) = (1 - q)/(1 + q),  q = exp(-2|v|/b)
 //   sigmoid(g) = 1/(1 + r) (g >= 0) or r/(1 + r) (g < 0),  r = exp(-|g|)
 // so the product is one quotient: no cancellation, no overflow, a few ulp.
+// The sigmoid of a large negative g is r itself, so r's relative error is
+// the result's: r comes from the accurate exp_neg, and for beta = 4
+// (kg = 1/2, the method's value) as qg^2 with qg = exp_neg(|g|/2) exact in
+// its argument, which saves an exponential.  qu's error only moves
+// tanh(|u|/b) by about qu times it (fast exponential).
 // kg = 2/beta, ku = 2/beta_lin, bb = beta*beta_lin.
 __device__ __forceinline__ float situ_f32(float g, float u, float kg, float ku, float bb) {
   const float ag = fabsf(g), au = fabsf(u);
-  float omg, qg, omu, qu;
-  one_minus_exp_neg(ag * kg, omg, qg);
-  one_minus_exp_neg(au * ku, omu, qu);
-  const float r = __expf(-ag);
+  const float xg = ag * kg, xu = au * ku;
+  const float qg = exp_neg(xg);
+  const float qu = __expf(-xu);
+  const float omg = one_minus_exp_neg(xg, qg);
+  const float omu = one_minus_exp_neg(xu, qu);
+  float r;
+  if (kg == 0.5f)
+    r = qg * qg;
+  else
+    r = exp_neg(ag);
   const float num = (omg * omu) * (g >= 0.0f ? 1.0f : r);
   const float den = ((1.0f + qg) * (1.0f + qu)) * (1.0f + r);
   const float mag = bb * __fdividef(num, den);
@@ -88,11 +125,16 @@ __device__ __forceinline__ float situ_f32(float g, float u, float kg, float ku, 
 // The clamped SwiGLU control: g' = min(g, limit), u' = clamp(u, -limit,
 // limit), out = g' * sigmoid(alpha*g') * (u' + beta), the sigmoid from the
 // exponential of a non-positive argument (1/(1+e) or e/(1+e), e = exp(-|z|)).
+// alpha*g' = z + zl exactly (zl from an fma); the sigmoid's relative error
+// grows like |z| times the error of z, so e is corrected by the factor
+// exp(-sign(z) zl) = 1 - sign(z) zl (|zl| <= 2^-24 |z|).
 __device__ __forceinline__ float swiglu_f32(float g, float u, float alpha, float beta, float limit) {
   const float gc = fminf(g, limit);
   const float uc = fminf(fmaxf(u, -limit), limit);
   const float z = alpha * gc;
-  const float e = __expf(-fabsf(z));
+  const float zl = fmaf(alpha, gc, -z);
+  float e = exp_neg(fabsf(z));
+  e = fmaf(e, z >= 0.0f ? -zl : zl, e);
   const float sig = __fdividef(z >= 0.0f ? 1.0f : e, 1.0f + e);
   return gc * sig * (uc + beta);
 }

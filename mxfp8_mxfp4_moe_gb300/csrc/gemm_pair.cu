@@ -154,6 +154,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
     if (!mbar_wait_bounded<true>(&item_full[sl], (li / kRing) & 1u, budget, a.err, abort_flag)) return -1;
     return item_w[sl];
   };
+  // the same, called by every lane of a converged warp
+  auto get_item_warp = [&](uint32_t li) -> int {
+    if (!C::DYN) {
+      const int w = pair + static_cast<int>(li) * npairs;
+      return w < total ? w : -1;
+    }
+    const uint32_t sl = li % kRing;
+    if (!mbar_wait_warp<true>(&item_full[sl], (li / kRing) & 1u, budget, a.err, abort_flag)) return -1;
+    return item_w[sl];
+  };
 
   if (warp == 0 || warp == C::PRODB_WARP) {
     // ------------------------------------------------------------ producers
@@ -250,12 +260,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && lead) {
+    if (lead) {
       // ---------------------------------------------------------- MMA issuer (even CTA)
-      // The tensor pipe takes the next MMA only about as fast as it runs one,
-      // so this loop stays lean: descriptors are formed once and advanced by
-      // adds (the start-address field holds smem offset >> 4), stage and
-      // phase advance incrementally, the item's MMA width comes from smem.
+      // The whole warp runs this loop converged and one elected lane issues
+      // each tcgen05 operation (ptx.cuh, the _el forms); the loop stays lean:
+      // descriptors are formed once and advanced by adds (the start-address
+      // field holds smem offset >> 4), stage and phase advance incrementally,
+      // the item's MMA width comes from smem.
       constexpr uint32_t kStageD = C::STAGE >> 4;
       constexpr uint32_t kAD = C::A_KB >> 4, kBD = C::B_BYTES >> 4;
       const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
@@ -267,15 +278,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       uint32_t ph = 0, slot = 0;
       bool ok = true;
       for (uint32_t li = 0; ok; ++li) {
-        if (get_item(li) < 0) break;
+        if (get_item_warp(li) < 0) break;
         const uint32_t acc = li & 1u;
-        if (!mbar_wait_bounded<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
+        if (!mbar_wait_warp<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * C::BN;
         uint32_t id0 = 0;
         bool two_chunks = false;
         for (int kb = 0; kb < a.KB; kb += C::KPS) {
-          if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&full[s], ph, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
@@ -290,16 +301,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
 #pragma unroll
           for (int kbi = 0; kbi < C::KPS; ++kbi) {
             const uint32_t sfa = sf + kbi * C::SFW;
-            tc_cp_32x128b_warpx4_pair(sfa, sfadesc0 + so + kbi * 32);
-            tc_cp_32x128b_warpx4_pair(sfa + 4, sfbdesc0 + so + kbi * C::NCH * 32);
-            if (two_chunks) tc_cp_32x128b_warpx4_pair(sfa + 8, sfbdesc0 + so + kbi * C::NCH * 32 + 32);
+            tc_cp_32x128b_warpx4_pair_el(sfa, sfadesc0 + so + kbi * 32);
+            tc_cp_32x128b_warpx4_pair_el(sfa + 4, sfbdesc0 + so + kbi * C::NCH * 32);
+            if (two_chunks) tc_cp_32x128b_warpx4_pair_el(sfa + 8, sfbdesc0 + so + kbi * C::NCH * 32 + 32);
             const uint64_t ad = adesc0 + so + kbi * kAD, bd = bdesc0 + so + kbi * kBD;
-            mma_mxf8f6f4_pair(d, ad, bd, id0, sfa, sfa + 4, (kb | kbi) != 0);
-            mma_mxf8f6f4_pair(d, ad + 2, bd + 2, id0 | (1u << 4) | (1u << 29), sfa, sfa + 4, 1u);
-            mma_mxf8f6f4_pair(d, ad + 4, bd + 4, id0 | (2u << 4) | (2u << 29), sfa, sfa + 4, 1u);
-            mma_mxf8f6f4_pair(d, ad + 6, bd + 6, id0 | (3u << 4) | (3u << 29), sfa, sfa + 4, 1u);
+            mma_mxf8f6f4_pair_el(d, ad, bd, id0, sfa, sfa + 4, (kb | kbi) != 0);
+            mma_mxf8f6f4_pair_el(d, ad + 2, bd + 2, id0 | (1u << 4) | (1u << 29), sfa, sfa + 4, 1u);
+            mma_mxf8f6f4_pair_el(d, ad + 4, bd + 4, id0 | (2u << 4) | (2u << 29), sfa, sfa + 4, 1u);
+            mma_mxf8f6f4_pair_el(d, ad + 6, bd + 6, id0 | (3u << 4) | (3u << 29), sfa, sfa + 4, 1u);
           }
-          tc_commit_pair(&empty[s]);
+          tc_commit_pair_el(&empty[s]);
           slot ^= C::SF_SLOT;
           if (++s == C::STAGES) {
             s = 0;
@@ -307,10 +318,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
           }
         }
         if (!ok) break;
-        tc_commit_pair(&acc_full[acc]);
+        tc_commit_pair_el(&acc_full[acc]);
       }
-      tc_commit_pair(done);
-      mbar_wait_bounded(done, 0, budget, a.err, nullptr);
+      tc_commit_pair_el(done);
+      mbar_wait_warp(done, 0, budget, a.err, nullptr);
     }
   } else if (warp < C::PRODB_WARP) {
     // ------------------------------------------------------------ epilogue

@@ -125,6 +125,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Fetch `bytes` (a multiple of 16, 16-byte aligned) from global memory into
+// L2 without a destination; completes on its own (nothing waits for it).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -339,6 +344,87 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
           smem_u32(bar)),
       "h"(static_cast<uint16_t>(3))
       : "memory");
+}
+
+// ------------------------------------------------- warp-converged issue
+// The forms below are executed by all 32 lanes of a converged warp; one
+// lane, chosen by elect.sync inside the same instruction sequence, issues
+// the operation.  Keeping the issuing warp converged (rather than running
+// the issue loop on one lane inside a divergent branch) lets the loop issue
+// tcgen05 operations several times faster: measured on GB300, four
+// block-scaled MMAs of N = 64 plus three scale copies take ~233 cycles per K
+// block this way against ~378 from a lone lane, and at N = 224 the three
+// copies cost nothing over the MMAs' own 474 cycles.
+__device__ __forceinline__ void mma_mxf8f6f4_el(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %6, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf8f6f4_pair_el(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                     uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %6, 0;\n"
+      " @e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_el(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n @e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}\n" ::"r"(
+          taddr),
+      "l"(sdesc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair_el(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n @e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n}\n" ::"r"(
+          taddr),
+      "l"(sdesc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_el(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_el(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n" ::"r"(
+          smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// Bounded wait executed by every lane of a converged warp: all lanes poll
+// and the warp leaves together (a vote per poll), so it stays converged for
+// the issue code that follows.  Same contract as mbar_wait_bounded.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint64_t budget_ns, uint32_t* err,
+                                               volatile int* abort) {
+  auto try_wait = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (__all_sync(0xffffffffu, try_wait())) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (__all_sync(0xffffffffu, try_wait())) return true;
+    if ((it & 63u) == 63u) {
+      const bool stop = (abort != nullptr && *abort) || (globaltimer_ns() - t0 > budget_ns);
+      if (__any_sync(0xffffffffu, stop)) {
+        if (lane_id() == 0 && !(abort != nullptr && *abort)) {
+          if (err) atomicOr(err, KMOE_DEVERR_TIMEOUT);
+          if (abort) *abort = 1;
+        }
+        __syncwarp();
+        return false;
+      }
+    }
+  }
 }
 
 // Named barrier among `nthreads` threads (multiple of 32).

@@ -56,24 +56,25 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A x B^T over K = 16 (32 bytes of each smem row).
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D[tmem] (+)= A x B^T over K = 16 (32 bytes of each smem row), executed by
+// every lane of a converged warp; one elected lane issues (see the
+// warp-converged forms in ptx.cuh).  The _pair form (M = 256, issued by the
+// even CTA): CTA r supplies A rows [128r, 128r+128) and B rows
+// [rN/2, (r+1)N/2) from its own shared memory; each CTA's TMEM gets its
+// 128 x N accumulator.
+__device__ __forceinline__ void mma_bf16_el(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-
-// The CTA-pair form (M = 256): CTA r supplies A rows [128r, 128r+128) and B
-// rows [rN/2, (r+1)N/2) from its own shared memory; each CTA's TMEM gets its
-// 128 x N accumulator.  Issued by the even CTA.
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16_pair_el(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -248,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop converged; one elected lane issues
+    {
       const uint32_t idesc = idesc_bf16(128, static_cast<uint32_t>(EN));
       const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
       const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + kATile));
@@ -261,30 +263,31 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
         const int nks = ((sp + 1) * kper < KS ? (sp + 1) * kper : KS) - sp * kper;
         const uint32_t acc = li & 1u;
         const uint32_t aph = (li >> 1) & 1u;
-        if (!mbar_wait_bounded(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
+        if (!mbar_wait_warp(&acc_empty[acc], aph ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * 256u;
         for (int ks = 0; ks < nks; ++ks) {
-          if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&full[s], ph, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t so = static_cast<uint64_t>(s) * static_cast<uint64_t>(stride >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(d, adesc0 + so + 2 * kk, bdesc0 + so + 2 * kk, idesc, (ks | kk) != 0);
-          tc_commit(&empty[s]);
+          mma_bf16_el(d, adesc0 + so, bdesc0 + so, idesc, ks != 0);
+          mma_bf16_el(d, adesc0 + so + 2, bdesc0 + so + 2, idesc, 1u);
+          mma_bf16_el(d, adesc0 + so + 4, bdesc0 + so + 4, idesc, 1u);
+          mma_bf16_el(d, adesc0 + so + 6, bdesc0 + so + 6, idesc, 1u);
+          tc_commit_el(&empty[s]);
           if (++s == nst) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&acc_full[acc]);
+        tc_commit_el(&acc_full[acc]);
       }
-      tc_commit(done);
-      mbar_wait_bounded(done, 0, budget, a.err, nullptr);
+      tc_commit_el(done);
+      mbar_wait_warp(done, 0, budget, a.err, nullptr);
     }
     __syncwarp();
   } else if (warp < kFirstRouteWarp) {
@@ -460,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (even CTA)
-    if (lane == 0 && lead) {
+    // the whole warp runs the loop converged; one elected lane issues
+    if (lead) {
       const uint32_t idesc = idesc_bf16(256, static_cast<uint32_t>(EN));
       const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
       const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + kATile));
@@ -469,30 +473,31 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
       bool ok = true;
       for (int it = pairi; it < items && ok; it += npairs, ++li) {
         const uint32_t acc = li & 1u;
-        if (!mbar_wait_bounded<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
+        if (!mbar_wait_warp<true>(&acc_empty[acc], ((li >> 1) & 1u) ^ 1u, budget, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * 256u;
         for (int ks = 0; ks < KS; ++ks) {
-          if (!mbar_wait_bounded(&full[s], ph, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&full[s], ph, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t so = static_cast<uint64_t>(s) * static_cast<uint64_t>(stride >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_pair(d, adesc0 + so + 2 * kk, bdesc0 + so + 2 * kk, idesc, (ks | kk) != 0);
-          tc_commit_pair(&empty[s]);
+          mma_bf16_pair_el(d, adesc0 + so, bdesc0 + so, idesc, ks != 0);
+          mma_bf16_pair_el(d, adesc0 + so + 2, bdesc0 + so + 2, idesc, 1u);
+          mma_bf16_pair_el(d, adesc0 + so + 4, bdesc0 + so + 4, idesc, 1u);
+          mma_bf16_pair_el(d, adesc0 + so + 6, bdesc0 + so + 6, idesc, 1u);
+          tc_commit_pair_el(&empty[s]);
           if (++s == nst) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair(&acc_full[acc]);
+        tc_commit_pair_el(&acc_full[acc]);
       }
-      tc_commit_pair(done);
-      mbar_wait_bounded(done, 0, budget, a.err, nullptr);
+      tc_commit_pair_el(done);
+      mbar_wait_warp(done, 0, budget, a.err, nullptr);
     }
     __syncwarp();
   } else if (warp < kFirstRouteWarp) {

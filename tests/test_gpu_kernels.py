@@ -153,12 +153,18 @@ def test_mma_peak_kernel_runs(K):
 ACT_REL_BOUND = 2.0 ** -18
 
 
+# (g, u) points at the end of the activation inputs; the first three have an
+# exact zero in g or u
+SPECIAL_GU = [(0.0, 3.0), (-0.0, 3.0), (5.0, 0.0), (1e-30, 1e-30), (4.0, 25.0), (-4.0, 25.0), (25.0, -4.0),
+              (-25.0, 4.0), (88.0, 1.0), (-88.0, 1.0), (1e30, 1e30), (-1e30, 1.0), (np.inf, 2.0),
+              (-np.inf, np.inf)]
+
+
 def _activation_inputs():
     rng = np.random.default_rng(11)
     parts = [rng.normal(0, 108, (2, 400000)), rng.normal(0, 14.5, (2, 400000)), rng.uniform(-40, 40, (2, 400000)),
              rng.uniform(-1, 1, (2, 200000)), rng.uniform(-1e-3, 1e-3, (2, 100000)),
-             np.array([[0.0, -0.0, 1e-30, 4.0, -4.0, 25.0, -25.0, 88.0, -88.0, 1e30, -1e30, np.inf, -np.inf],
-                       [3.0, 3.0, 1e-30, 25.0, 25.0, -4.0, 4.0, 1.0, 1.0, 1e30, 1.0, 2.0, np.inf]])]
+             np.array(SPECIAL_GU).T]
     gu = np.concatenate(parts, axis=1).astype(np.float32)
     return gu[0], gu[1]
 
@@ -177,10 +183,13 @@ def test_activation_error_bound(K, act, params):
     p = K.make_params(0, 128, 128, 1, 1, activation=act, **params)
     out = K.kmoe_selftest_activation(p, torch.from_numpy(g).cuda(), torch.from_numpy(u).cuda()).cpu().numpy()
     gd, ud = g.astype(np.float64), u.astype(np.float64)
+    # the library receives the parameters as fp32 (kmoe_params): the oracle
+    # evaluates the formula in double with those same values
+    f32 = {n: float(np.float32(v)) for n, v in params.items()}
     if act == "situ":
-        ref = O.situ(gd, ud, params["situ_beta"], params["situ_linear_beta"])
+        ref = O.situ(gd, ud, f32["situ_beta"], f32["situ_linear_beta"])
     else:
-        ref = O.swiglu(gd, ud, params["swiglu_alpha"], params["swiglu_beta"], params["swiglu_limit"])
+        ref = O.swiglu(gd, ud, f32["swiglu_alpha"], f32["swiglu_beta"], f32["swiglu_limit"])
     assert np.all(np.isfinite(out))
     big = np.abs(ref) > 1e-30
     rel = np.abs(out[big].astype(np.float64) - ref[big]) / np.abs(ref[big])
@@ -191,4 +200,5 @@ def test_activation_error_bound(K, act, params):
     assert tiny_abs <= 1e-30
     # exact zeros stay zero (SiTU(0, u) = SiTU(g, 0) = 0)
     if act == "situ":
-        assert out[0] == 0.0 and out[1] == 0.0
+        n0 = len(out) - len(SPECIAL_GU)
+        assert out[n0] == 0.0 and out[n0 + 1] == 0.0 and out[n0 + 2] == 0.0
