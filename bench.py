@@ -214,6 +214,29 @@ def fc1_traffic_record():
     return rec
 
 
+DECODE_KERNEL_SOURCES = ("gemm.cu", "gemm_dev.cuh", "gemm.cuh", "ptx.cuh")
+
+
+def decode_kernel_sha256():
+    """sha256 over the sources of the small-tile (decode) GEMM kernel."""
+    h = hashlib.sha256()
+    for f in DECODE_KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "mxfp8_mxfp4_moe_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def decode_traffic_record():
+    """DRAM bytes per touched expert of the decode FC1 launch from a committed
+    ncu summary, if the kernel sources are unchanged since (else null)."""
+    path = os.path.join(ROOT, "profiles", "decode_fc1_dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    if rec.get("decode_kernel_sha256") != decode_kernel_sha256():
+        return None
+    return rec
+
+
 # ----------------------------------------------------------------------------- layer set-up
 class Layer:
     def __init__(self, w: W.Workload, device, weights=None):
@@ -679,6 +702,7 @@ def run_ours(args):
     d_fc1_gbs = touched * per_expert_w13 / (d_stages[3] / 1e3) / 1e9
     d_layer_gbs = configs[DECODE]["layer_GBs"]
     d_graph_us = time_graph(dl, 20)
+    d_traffic = decode_traffic_record()
     dl.check()
     del dl, layers, flush
     torch.cuda.empty_cache()
@@ -805,7 +829,8 @@ def run_ours(args):
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": d_fc1_gbs / peaks["hbm_gbs"],
                                     "algorithmic": f"touched experts x {per_expert_w13} B of w13 codes+scales",
-                                    "traffic": None}},
+                                    "traffic": (touched * d_traffic["dram_bytes_per_touched_expert"]
+                                                if d_traffic else None)}},
             "e2e": {"value": e2e_tok_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": gpu_launches,
             "clocks": clk,
