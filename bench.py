@@ -672,7 +672,7 @@ def run_ours(args):
             "tflops": w_.flops() / (m / 1e3) / 1e12, "fp8_frac": w_.flops() / (m / 1e3) / 1e12 / fp8_peak,
             "touched_experts": touched, "algorithmic_bytes": alg, "layer_GBs": alg / (m / 1e3) / 1e9,
             "hbm_frac": alg / (m / 1e3) / 1e9 / peaks["hbm_gbs"],
-            "tile_rows": K.kmoe_workspace_layout(L.p).tile_rows,
+            "tile_rows": tile_classes(K, L.p),
             "rounds_ms": rounds[n], "forwards_per_round": [c for c in counts[n] if c],
             "timing": ("each forward timed alone after a write of 2 x L2 (inputs fit in L2)" if n in FLUSHED
                        else "back-to-back forwards (weights larger than L2)")}
@@ -887,8 +887,15 @@ def run_profile(args):
     import mxfp8_mxfp4_moe_gb300 as K
     print(json.dumps({"profile": w.name, "stages_ms": dict(zip(K.STAGE_NAMES, layer.stage_ms())),
                       "touched_experts": layer.touched_experts(),
-                      "tile_rows": K.kmoe_workspace_layout(layer.p).tile_rows}))
+                      "tile_rows": tile_classes(K, layer.p)}))
     return 0
+
+
+def tile_classes(K, p):
+    """Token-tile sizes of a layer: small tiles for experts with at most
+    big_rows rows, big (CTA-pair) tiles for the others (0: none possible)."""
+    L = K.kmoe_workspace_layout(p)
+    return {"small": L.tile_rows, "big": L.tile_rows_big, "big_above_rows": L.big_rows}
 
 
 def layer_params(K, w):

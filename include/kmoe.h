@@ -116,7 +116,7 @@ typedef struct kmoe_ws_layout {
   size_t topk_w;       /* float [T, k] routing weights used */
   size_t counts;       /* int32 [E] rows per expert */
   size_t seg_start;    /* int32 [E+1] first expert-sorted row of each expert */
-  size_t tile_start;   /* int32 [E+1] first tile of each expert */
+  size_t tile_start;   /* int32 [E+1] first small tile of each expert (prefix over the small-tile experts) */
   size_t row_of_slot;  /* int32 [T*k] expert-sorted row of slot t*k+j (-1 if masked) */
   size_t slot_of_row;  /* int32 [R] slot t*k+j of each expert-sorted row */
   size_t xq;           /* uint8 [R, H] E4M3 codes of x, expert-sorted */
@@ -124,10 +124,20 @@ typedef struct kmoe_ws_layout {
   size_t iq;           /* uint8 [R, I] E4M3 codes of the FC1 activation, expert-sorted */
   size_t isf;          /* uint8 tile-layout UE8M0 scales of iq */
   size_t y;            /* float [T*k, H] per-slot FC2 outputs (slot order) */
-  int tile_rows;       /* rows per token tile (BN) chosen for these parameters */
-  int max_tiles;       /* capacity of the tile-layout scale arrays, in tiles */
+  int tile_rows;       /* rows per small token tile (32 or 64) chosen for these parameters */
+  int max_tiles;       /* capacity of the small-tile scale arrays (xsf, isf), in tiles */
   size_t total;        /* == kmoe_workspace_size(p) */
   size_t logits;       /* float [T, E] router logits (written by kmoe_forward_router) */
+  /* Experts with more than big_rows rows are cut into tiles of tile_rows_big
+   * rows with their own numbering and scale arrays; the others into small
+   * tiles.  tile_rows_big is 0 when no expert can have more than big_rows
+   * rows (T <= big_rows): every tile is then small. */
+  size_t tile_start_big; /* int32 [E+1] first big tile of each expert (prefix over the big-tile experts) */
+  size_t xsf_big;      /* uint8 tile-layout scales of xq rows in big tiles */
+  size_t isf_big;      /* uint8 tile-layout scales of iq rows in big tiles */
+  int tile_rows_big;   /* 224, or 0 (see above) */
+  int max_tiles_big;   /* capacity of xsf_big / isf_big, in tiles */
+  int big_rows;        /* row-count threshold of the big tiles */
 } kmoe_ws_layout;
 int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out /* host */);
 
@@ -255,10 +265,11 @@ int kmoe_forward_router(const kmoe_params* p, const void* x_bf16, const void* w_
  * it reports the most recent forward on that workspace. */
 int kmoe_device_error(void* workspace, uint32_t* word, cudaStream_t stream);
 
-/* Byte offset, inside a tile-layout scale array (xsf/isf of the workspace),
- * of the scale of row `local_row` of token tile `tile` for 32-group `g`
- * (K index 32g..32g+31), given the tile size, the K width in elements and the
- * tile capacity of the array.  Host helper for inspection. */
+/* Byte offset, inside a tile-layout scale array (xsf/isf, or xsf_big/isf_big,
+ * of the workspace), of the scale of row `local_row` of token tile `tile` for
+ * 32-group `g` (K index 32g..32g+31), given the array's tile size (tile_rows
+ * or tile_rows_big), the K width in elements and the tile capacity of the
+ * array.  Host helper for inspection. */
 size_t kmoe_tile_sf_offset(int tile, int local_row, int g, int tile_rows, int K, int max_tiles);
 
 /* Measurement aid: the tensor-pipe roof of the instruction the expert GEMMs

@@ -42,7 +42,9 @@ class kmoe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("err", "topk_ids", "topk_w", "counts", "seg_start", "tile_start",
                                                "row_of_slot", "slot_of_row", "xq", "xsf", "iq", "isf", "y")] + \
                [("tile_rows", ctypes.c_int), ("max_tiles", ctypes.c_int), ("total", ctypes.c_size_t),
-                ("logits", ctypes.c_size_t)]
+                ("logits", ctypes.c_size_t), ("tile_start_big", ctypes.c_size_t), ("xsf_big", ctypes.c_size_t),
+                ("isf_big", ctypes.c_size_t), ("tile_rows_big", ctypes.c_int), ("max_tiles_big", ctypes.c_int),
+                ("big_rows", ctypes.c_int)]
 
 
 class kmoe_stage_events(ctypes.Structure):
@@ -413,6 +415,9 @@ def stage_views(p, workspace):
         "iq": v(L.iq, R * p.I, torch.uint8).view(R, p.I),
         "xsf": workspace[L.xsf:L.xsf + (p.H // 128) * L.max_tiles * ((L.tile_rows + 127) // 128) * 512],
         "isf": workspace[L.isf:L.isf + (p.I // 128) * L.max_tiles * ((L.tile_rows + 127) // 128) * 512],
+        "tile_start_big": v(L.tile_start_big, p.E + 1, torch.int32),
+        "xsf_big": workspace[L.xsf_big:L.xsf_big + (p.H // 128) * L.max_tiles_big * 2 * 512],
+        "isf_big": workspace[L.isf_big:L.isf_big + (p.I // 128) * L.max_tiles_big * 2 * 512],
         "y": v(L.y, R * p.H, torch.float32).view(R, p.H),
         "logits": v(L.logits, p.T * p.E, torch.float32).view(p.T, p.E),
     }

@@ -13,12 +13,12 @@
 
 namespace kmoe {
 cudaError_t launch_route(const float*, const float*, int, int, int, int32_t*, float*, cudaStream_t);
-cudaError_t launch_permute(const int32_t*, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
-                           uint32_t*, cudaStream_t);
+cudaError_t launch_permute(const int32_t*, int, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
+                           int32_t*, uint32_t*, cudaStream_t);
 cudaError_t launch_quant_rows(const void*, int, int, int, uint8_t*, uint8_t*, cudaStream_t);
-cudaError_t launch_quant_scatter(const void*, int, int, int, int, int, int, int, const int32_t*, const int32_t*,
-                                 const int32_t*, const int32_t*, const int32_t*, int32_t*, int32_t*, uint8_t*,
-                                 uint8_t*, cudaStream_t);
+cudaError_t launch_quant_scatter(const void*, int, int, int, int, int, int, const int32_t*, const int32_t*,
+                                 const int32_t*, const int32_t*, const int32_t*, const int32_t*, const int32_t*,
+                                 int32_t*, int32_t*, uint8_t*, uint8_t*, uint8_t*, cudaStream_t);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int, int, int, int, float, void*,
                            cudaStream_t);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t budget_ns, cudaStream_t st);
@@ -224,6 +224,12 @@ int kmoe_workspace_layout(const kmoe_params* p, kmoe_ws_layout* out) {
   out->max_tiles = L.max_tiles;
   out->total = L.total;
   out->logits = L.logits;
+  out->tile_start_big = L.tile_start_big;
+  out->xsf_big = L.xsf_big;
+  out->isf_big = L.isf_big;
+  out->tile_rows_big = L.big ? kBigTileRows : 0;
+  out->max_tiles_big = L.max_tiles_big;
+  out->big_rows = kBigRows;
   return KMOE_OK;
 }
 
@@ -317,30 +323,42 @@ static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* l
   float* y = reinterpret_cast<float*>(ws + L.y);
   const int T = p->T, H = p->H, I = p->I, E = p->E, k = p->k, R = L.R;
 
-  // tensor maps: weights as E2M1 (unpacked to 16-byte aligned groups in smem), token rows as bytes
+  int32_t* tile_start_big = reinterpret_cast<int32_t*>(ws + L.tile_start_big);
+  uint8_t* xsf_big = ws + L.xsf_big;
+  uint8_t* isf_big = ws + L.isf_big;
+  // experts with more rows than `thr` take the big tiles (none when no expert can)
+  const int thr = L.big ? kBigRows : 0x7fffffff;
+
+  // Tensor maps of one tile class: weights as E2M1 (unpacked to 16-byte
+  // aligned groups in smem), token rows as bytes in boxes of 32, 64, 128, a
+  // tile and half a tile of rows, and (CTA-pair kernel) the weight and token
+  // scale regions as rows of 128 bytes.
+  auto class_maps = [&](GemmMaps& m, const uint8_t* w_k, int which, int kps, const uint8_t* act, int K,
+                        const uint8_t* sf, int bn, int max_tiles) -> bool {
+    const int nch = (bn + 127) / 128;
+    const uint64_t nblk = weight_blocks(p, which);
+    if (!make_weight_map(&m.a, w_k, nblk, kps)) return false;
+    if (!make_map(&m.asf, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_k + nblk * 8192, 128, nblk * 4, 128, 128, 4, false))
+      return false;
+    const uint64_t sf_rows = static_cast<uint64_t>(K / 128) * (max_tiles > 0 ? max_tiles : 1) * nch * 4;
+    if (!make_map(&m.bsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, sf, 128, sf_rows, 128, 128, 4 * nch, false)) return false;
+    for (int i = 0; i < 5; ++i) {
+      const uint32_t rows = i < 3 ? (32u << i) : static_cast<uint32_t>(i == 3 ? bn : bn / 2);
+      if (!make_map(&m.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, act, K, R, K, 128, rows)) return false;
+    }
+    return true;
+  };
   const int kps1 = gemm_kblocks_per_stage(L.BN, H / 128);
   const int kps2 = gemm_kblocks_per_stage(L.BN, I / 128);
-  GemmMaps m1, m2;
-  if (!make_weight_map(&m1.a, w13_k, weight_blocks(p, 0), kps1) ||
-      !make_weight_map(&m2.a, w2_k, weight_blocks(p, 1), kps2))
+  const int kpsb1 = gemm_kblocks_per_stage(kBigTileRows, H / 128);
+  const int kpsb2 = gemm_kblocks_per_stage(kBigTileRows, I / 128);
+  GemmMaps m1, m2, mb1, mb2;
+  if (!class_maps(m1, w13_k, 0, kps1, xq, H, xsf, L.BN, L.max_tiles) ||
+      !class_maps(m2, w2_k, 1, kps2, iq, I, isf, L.BN, L.max_tiles))
     return KMOE_ERR_CUDA;
-  // the scale regions as rows of 128 bytes (the CTA-pair kernel loads them by TMA)
-  const uint64_t sf1_rows = static_cast<uint64_t>(H / 128) * L.max_tiles * L.nch * 4;
-  const uint64_t sf2_rows = static_cast<uint64_t>(I / 128) * L.max_tiles * L.nch * 4;
-  if (!make_map(&m1.asf, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13_k + weight_blocks(p, 0) * 8192, 128,
-                weight_blocks(p, 0) * 4, 128, 128, 4, false) ||
-      !make_map(&m2.asf, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2_k + weight_blocks(p, 1) * 8192, 128,
-                weight_blocks(p, 1) * 4, 128, 128, 4, false) ||
-      !make_map(&m1.bsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, xsf, 128, sf1_rows, 128, 128, 4 * L.nch, false) ||
-      !make_map(&m2.bsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, isf, 128, sf2_rows, 128, 128, 4 * L.nch, false))
+  if (L.big && (!class_maps(mb1, w13_k, 0, kpsb1, xq, H, xsf_big, kBigTileRows, L.max_tiles_big) ||
+                !class_maps(mb2, w2_k, 1, kpsb2, iq, I, isf_big, kBigTileRows, L.max_tiles_big)))
     return KMOE_ERR_CUDA;
-  for (int i = 0; i < 5; ++i) {
-    // 32, 64, 128 rows, one tile, half a tile
-    const uint32_t rows = i < 3 ? (32u << i) : static_cast<uint32_t>(i == 3 ? L.BN : L.BN / 2);
-    if (!make_map(&m1.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, H, R, H, 128, rows) ||
-        !make_map(&m2.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, iq, I, R, I, 128, rows))
-      return KMOE_ERR_CUDA;
-  }
 
   auto mark = [&](cudaEvent_t e) { return (ev && e) ? cudaEventRecord(e, stream) : cudaSuccess; };
   KMOE_CK(mark(ev ? ev->start : nullptr));
@@ -358,24 +376,42 @@ static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* l
     KMOE_CK(launch_route(logits, bias, T, E, k, ids, wts, stream));
   }
   KMOE_CK(mark(ev ? ev->routed : nullptr));
-  KMOE_CK(launch_permute(ids, R, E, L.BN, rank, chunk_prefix, counts, seg_start, tile_start, err, stream));
+  KMOE_CK(launch_permute(ids, R, E, L.BN, thr, rank, chunk_prefix, counts, seg_start, tile_start, tile_start_big, err,
+                         stream));
   KMOE_CK(mark(ev ? ev->permuted : nullptr));
-  KMOE_CK(launch_quant_scatter(x_bf16, T, H, k, E, L.BN, L.nch, L.max_tiles, ids, rank, chunk_prefix, seg_start,
-                               tile_start, row_of_slot, slot_of_row, xq, xsf, stream));
+  KMOE_CK(launch_quant_scatter(x_bf16, T, H, k, E, L.BN, thr, ids, rank, chunk_prefix, counts, seg_start, tile_start,
+                               tile_start_big, row_of_slot, slot_of_row, xq, xsf, xsf_big, stream));
   KMOE_CK(mark(ev ? ev->quantized : nullptr));
   const int grid = num_sms();
   if (grid <= 0) return KMOE_ERR_CUDA;
+  // FC1 and FC2 each run the big-tile experts (CTA pairs) and then the
+  // small-tile experts; the two launches cover disjoint experts and rows
   GemmArgs a1{counts, seg_start, tile_start, w13_k, w13_k + weight_blocks(p, 0) * 8192, xsf, E, I / 64, H / 128,
               L.max_tiles, H, I, iq, isf, static_cast<float>(2.0 / p->situ_beta),
               static_cast<float>(2.0 / p->situ_linear_beta),
               static_cast<float>(static_cast<double>(p->situ_beta) * p->situ_linear_beta), nullptr, slot_of_row,
               err, kWaitBudgetNs, reinterpret_cast<int*>(err) + 2,
               (p->flags & KMOE_FLAG_SWIGLU) ? 1 : 0, p->swiglu_alpha, p->swiglu_beta, p->swiglu_limit};
+  if (L.big) {
+    GemmArgs ab1 = a1;
+    ab1.tile_start = tile_start_big;
+    ab1.bsf = xsf_big;
+    ab1.isf = isf_big;
+    ab1.max_tiles = L.max_tiles_big;
+    KMOE_CK(launch_moe_gemm(true, kBigTileRows, kpsb1, mb1, ab1, grid, stream));
+  }
   KMOE_CK(launch_moe_gemm(true, L.BN, kps1, m1, a1, grid, stream));
   KMOE_CK(mark(ev ? ev->fc1 : nullptr));
   GemmArgs a2{counts, seg_start, tile_start, w2_k, w2_k + weight_blocks(p, 1) * 8192, isf, E, H / 128, I / 128,
               L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs,
               reinterpret_cast<int*>(err) + 3, 0, 0.f, 0.f, 0.f};
+  if (L.big) {
+    GemmArgs ab2 = a2;
+    ab2.tile_start = tile_start_big;
+    ab2.bsf = isf_big;
+    ab2.max_tiles = L.max_tiles_big;
+    KMOE_CK(launch_moe_gemm(false, kBigTileRows, kpsb2, mb2, ab2, grid, stream));
+  }
   KMOE_CK(launch_moe_gemm(false, L.BN, kps2, m2, a2, grid, stream));
   KMOE_CK(mark(ev ? ev->fc2 : nullptr));
   KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));

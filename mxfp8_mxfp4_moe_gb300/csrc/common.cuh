@@ -127,19 +127,30 @@ __host__ inline size_t router_part_bytes(const RouterPlan& r, int T, int E) {
 }
 
 // ---------------------------------------------------------------- workspace
+// Token tiles come in two classes, chosen per expert from its row count:
+// experts with at most kBigRows rows are cut into small tiles of BN (32 or
+// 64) rows, run by the one-CTA kernel (two CTAs per SM) that streams their
+// weights at HBM speed; experts with more rows are cut into 224-row tiles,
+// run by the CTA-pair kernel, where the tensor pipe is the limit.  Each class
+// has its own tile numbering (tile_start / tile_start_big, prefixes over the
+// experts in order) and its own token-tile scale arrays.
+constexpr int kBigRows = 64;
+constexpr int kBigTileRows = 224;
+
 struct Layout {
   size_t err, topk_ids, topk_w, counts, seg_start, tile_start, chunk_prefix, rank, row_of_slot, slot_of_row;
   size_t xq, xsf, iq, isf, y, logits, router_sync, router_part, total;
+  size_t tile_start_big, xsf_big, isf_big;
   int R, BN, nch, max_tiles, nchunk;
+  int big;        // 1 if an expert can exceed kBigRows rows (T > kBigRows), else no big tiles
+  int max_tiles_big;
 };
 
-// Token-tile size for a layer: small tiles when few rows reach each expert
-// (decode), large tiles when many do (prefill).
+// Small-tile size for a layer: 32 rows when few rows reach each expert on
+// average (decode), else 64.
 __host__ inline int choose_tile_rows(long long R, int E) {
   const double avg = static_cast<double>(R) / E;
-  if (avg <= 20.0) return 32;
-  if (avg <= 48.0) return 64;
-  return 224;
+  return avg <= 20.0 ? 32 : 64;
 }
 
 __host__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -149,9 +160,16 @@ __host__ inline bool make_layout(const kmoe_params& p, Layout& L) {
   const size_t R = static_cast<size_t>(p.T) * p.k;
   L.R = static_cast<int>(R);
   L.BN = choose_tile_rows(static_cast<long long>(R), p.E);
-  L.nch = (L.BN + 127) / 128;
-  L.max_tiles = static_cast<int>((R + L.BN - 1) / L.BN + (R < static_cast<size_t>(p.E) ? R : p.E));
+  L.nch = 1;
+  // an expert has at most T rows (one per token)
+  L.big = p.T > kBigRows ? 1 : 0;
+  const size_t nE = static_cast<size_t>(p.E);
+  const size_t small_cap = L.big ? nE * ((kBigRows + L.BN - 1) / L.BN) : (R + L.BN - 1) / L.BN + (R < nE ? R : nE);
+  const size_t small_all = (R + L.BN - 1) / L.BN + (R < nE ? R : nE);
+  L.max_tiles = static_cast<int>(small_cap < small_all ? small_cap : small_all);
   if (L.max_tiles < 1) L.max_tiles = 1;
+  const size_t nbig = R / (kBigRows + 1) < nE ? R / (kBigRows + 1) : nE;  // experts with > kBigRows rows
+  L.max_tiles_big = L.big ? static_cast<int>((R + kBigTileRows - 1) / kBigTileRows + nbig) : 0;
   L.nchunk = static_cast<int>((R + kRankChunk - 1) / kRankChunk);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -173,6 +191,9 @@ __host__ inline bool make_layout(const kmoe_params& p, Layout& L) {
   L.xsf = take(static_cast<size_t>(p.H / 128) * L.max_tiles * L.nch * 512);
   L.iq = take(R * p.I);
   L.isf = take(static_cast<size_t>(p.I / 128) * L.max_tiles * L.nch * 512);
+  L.tile_start_big = take(static_cast<size_t>(p.E + 1) * 4);
+  L.xsf_big = take(static_cast<size_t>(p.H / 128) * L.max_tiles_big * 2 * 512);
+  L.isf_big = take(static_cast<size_t>(p.I / 128) * L.max_tiles_big * 2 * 512);
   L.y = take(R * p.H * 4);
   // the fused router's outputs and counters (token counter, one per 128-token tile)
   L.logits = take(static_cast<size_t>(p.T) * p.E * 4);

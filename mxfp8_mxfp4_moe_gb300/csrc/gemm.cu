@@ -18,7 +18,8 @@
 // 8192 code bytes (128 rows x 64 B) followed by its 512 scale bytes, blocks
 // ordered by K block.  A work item therefore streams one contiguous range.
 //
-// Warp roles (persistent; one CTA per SM, two for the 32-row decode tiles):
+// Warp roles (persistent; one CTA per SM for the 224-row tiles, two for the
+// 32- and 64-row tiles):
 //   warp 0      TMA producer of the weight codes and scales (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..   epilogue, EPI_WARPS in groups of four; warp w reads TMEM lane
@@ -404,16 +405,14 @@ cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, con
   if (fc1) {
     if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, true, 4, 2, 1, PF>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<32, 1, 8, true, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
-    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 3, true, 8, 1, 1, PF>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<64, 1, 6, true, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
+    if (BN == 64 && kps == 1) return launch_one<GemmCfg<64, 1, 3, true, 4, 2, 1, 2 * PF>>(maps, a, grid, st);
     if (BN == 224 && kps == 1)
       return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(true, maps, a, grid, st)
                            : launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
   } else {
     if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2, 1, PF>>(maps, a, grid, st)
                                   : launch_one<GemmCfg<32, 1, 8, false, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
-    if (BN == 64) return kps == 2 ? launch_one<GemmCfg<64, 2, 4, false, 8, 1, 1, PF>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<64, 1, 7, false, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
+    if (BN == 64 && kps == 1) return launch_one<GemmCfg<64, 1, 4, false, 4, 2, 1, 2 * PF>>(maps, a, grid, st);
     if (BN == 224 && kps == 1)
       return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(false, maps, a, grid, st)
                            : launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st);

@@ -19,8 +19,9 @@ struct GemmMaps {
 };
 
 // K blocks (of 128) moved per pipeline stage for a token-tile size and a K
-// of KB blocks: two for the small tiles when KB is even, else one.
-inline int gemm_kblocks_per_stage(int BN, int KB) { return (BN <= 64 && KB % 2 == 0) ? 2 : 1; }
+// of KB blocks: two for the 32-row tiles when KB is even, else one (the
+// 64-row tiles run two CTAs per SM with single-K-block stages).
+inline int gemm_kblocks_per_stage(int BN, int KB) { return (BN <= 32 && KB % 2 == 0) ? 2 : 1; }
 
 struct GemmArgs {
   const int32_t* counts;      // [E]

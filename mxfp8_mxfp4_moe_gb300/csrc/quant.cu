@@ -106,7 +106,9 @@ cudaError_t launch_quant_rows(const void* x, int rows, int cols, int fmt, uint8_
 }
 
 // One block per token.  Threads 0..k-1 first resolve the token's k slots to
-// expert-sorted rows and token tiles; then each thread quantises one
+// expert-sorted rows and token tiles (of the expert's tile class: BN rows for
+// experts with at most `thr` rows, kBigTileRows rows and the xsf_big scale
+// array for the others); then each thread quantises one
 // 32-element group.  A warp's 32 groups form one contiguous 1 KB run of code
 // bytes per routed slot: the lanes exchange their codes once (shuffles) so
 // that each store instruction writes 512 contiguous bytes (lane l: 16-byte
@@ -115,30 +117,33 @@ cudaError_t launch_quant_rows(const void* x, int rows, int cols, int fmt, uint8_
 // scale bytes are adjacent in the token-tile scale layout, so the quad merges
 // them and its first lane writes one 32-bit word per slot.
 __global__ void __launch_bounds__(256) quant_scatter_kernel(
-    const __nv_bfloat16* __restrict__ x, int H, int k, int E, int BN, int nch, int max_tiles,
-    const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, const int32_t* __restrict__ chunk_prefix,
+    const __nv_bfloat16* __restrict__ x, int H, int k, int E, int BN, int thr, const int32_t* __restrict__ ids,
+    const int32_t* __restrict__ rank, const int32_t* __restrict__ chunk_prefix, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ seg_start, const int32_t* __restrict__ tile_start,
-    int32_t* __restrict__ row_of_slot, int32_t* __restrict__ slot_of_row, uint8_t* __restrict__ xq,
-    uint8_t* __restrict__ xsf) {
-  __shared__ int s_row[kMaxK], s_tile[kMaxK], s_local[kMaxK];
+    const int32_t* __restrict__ tile_start_big, int32_t* __restrict__ row_of_slot, int32_t* __restrict__ slot_of_row,
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, uint8_t* __restrict__ xsf_big) {
+  __shared__ int s_row[kMaxK], s_tile[kMaxK], s_local[kMaxK], s_big[kMaxK];
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     const int j = threadIdx.x;
     const int s = t * k + j;
     const int id = ids[s];
-    int row = -1, tile = -1, local = -1;
+    int row = -1, tile = -1, local = -1, big = 0;
     if (id >= 0 && id < E) {
       const int c = s / kRankChunk;
       const int in_seg = chunk_prefix[static_cast<size_t>(c) * E + id] + rank[s];
       row = seg_start[id] + in_seg;
-      tile = tile_start[id] + in_seg / BN;
-      local = in_seg % BN;
+      big = counts[id] > thr;
+      const int bn = big ? kBigTileRows : BN;
+      tile = (big ? tile_start_big[id] : tile_start[id]) + in_seg / bn;
+      local = in_seg % bn;
       slot_of_row[row] = s;
     }
     row_of_slot[s] = row;
     s_row[j] = row;
     s_tile[j] = tile;
     s_local[j] = local;
+    s_big[j] = big;
   }
   __syncthreads();
   const int lane = static_cast<int>(threadIdx.x) & 31;
@@ -181,20 +186,24 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
       uint4* run = reinterpret_cast<uint4*>(xq + static_cast<size_t>(row) * H + 32 * gw);
       if (st0) run[lane] = v0;
       if (st1) run[32 + lane] = v1;
-      if (active && (g & 3) == 0)
-        *reinterpret_cast<uint32_t*>(xsf + tile_sf_offset(s_tile[j], s_local[j], g, nch, KB)) = sc;
+      if (active && (g & 3) == 0) {
+        // small tiles (at most 64 rows) hold one 128-row scale chunk, big tiles two
+        uint8_t* base = s_big[j] ? xsf_big : xsf;
+        *reinterpret_cast<uint32_t*>(base + tile_sf_offset(s_tile[j], s_local[j], g, s_big[j] ? 2 : 1, KB)) = sc;
+      }
     }
   }
 }
 
-cudaError_t launch_quant_scatter(const void* x, int T, int H, int k, int E, int BN, int nch, int max_tiles,
-                                 const int32_t* ids, const int32_t* rank, const int32_t* chunk_prefix,
-                                 const int32_t* seg_start, const int32_t* tile_start, int32_t* row_of_slot,
-                                 int32_t* slot_of_row, uint8_t* xq, uint8_t* xsf, cudaStream_t st) {
+cudaError_t launch_quant_scatter(const void* x, int T, int H, int k, int E, int BN, int thr, const int32_t* ids,
+                                 const int32_t* rank, const int32_t* chunk_prefix, const int32_t* counts,
+                                 const int32_t* seg_start, const int32_t* tile_start, const int32_t* tile_start_big,
+                                 int32_t* row_of_slot, int32_t* slot_of_row, uint8_t* xq, uint8_t* xsf,
+                                 uint8_t* xsf_big, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  quant_scatter_kernel<<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), H, k, E, BN, nch, max_tiles, ids,
-                                          rank, chunk_prefix, seg_start, tile_start, row_of_slot, slot_of_row, xq,
-                                          xsf);
+  quant_scatter_kernel<<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), H, k, E, BN, thr, ids, rank,
+                                          chunk_prefix, counts, seg_start, tile_start, tile_start_big, row_of_slot,
+                                          slot_of_row, xq, xsf, xsf_big);
   return cudaGetLastError();
 }
 

@@ -125,13 +125,16 @@ def oracle_forward_pool(w, s, tokens, ids=None, topk_w=None, workers=None):
     return {"out": out, "inter_q": iq, "inter_s": isf, "y": y, "ids": ids, "topk_w": topk_w}
 
 
-def tile_position_tokens(ids: np.ndarray, E: int, BN: int, n: int = 32, seed: int = 0):
+def tile_position_tokens(ids: np.ndarray, E: int, BN: int, n: int = 32, seed: int = 0, big_rows: int = 0,
+                         BN_big: int = 0):
     """Tokens chosen by where their rows land in the expert-sorted token
-    tiles of BN rows (rows of an expert in slot order, as the permutation
-    lays them out): for the three most- and three least-loaded experts and
-    the last expert with rows (whose work items are claimed last), the first
-    row, the rows on both sides of the first tile boundary, a middle row and
-    the last row (the partial tile); then random tokens up to n."""
+    tiles (rows of an expert in slot order, as the permutation lays them
+    out; tiles of BN rows, or of BN_big rows for experts with more than
+    big_rows rows when BN_big > 0): for the three most- and three
+    least-loaded experts and the last expert with rows (whose work items are
+    claimed last), the first row, the rows on both sides of the first tile
+    boundary, a middle row and the last row (the partial tile); then random
+    tokens up to n."""
     T, k = ids.shape
     flat = ids.ravel()
     valid = flat >= 0
@@ -144,9 +147,10 @@ def tile_position_tokens(ids: np.ndarray, E: int, BN: int, n: int = 32, seed: in
     toks = set()
     for e in chosen:
         c = int(counts[e])
-        nt = (c + BN - 1) // BN
-        mid = (nt // 2) * BN + (min(BN, c - (nt // 2) * BN) // 2)
-        rows = {0, mid, c - 1} | ({BN - 1, BN} if nt > 1 else set())
+        bn = BN_big if (BN_big > 0 and c > big_rows) else BN
+        nt = (c + bn - 1) // bn
+        mid = (nt // 2) * bn + (min(bn, c - (nt // 2) * bn) // 2)
+        rows = {0, mid, c - 1} | ({bn - 1, bn} if nt > 1 else set())
         for r in rows:
             toks.add(int(order[starts[e] + r] // k))
     rng = np.random.default_rng(seed)
@@ -181,20 +185,31 @@ def tile_sf_offsets(tile, local, g, BN, KB):
     return ((tile * KB + kb) * nch + chunk) * 512 + (r % 32) * 16 + (r // 32) * 4 + (g % 4)
 
 
-def gather_row_scales(sf_bytes: np.ndarray, views_np, rows: np.ndarray, K: int):
-    """Scales [len(rows), K/32] of expert-sorted rows from a token-tile scale array."""
+def gather_row_scales(views_np, which: str, rows: np.ndarray, K: int):
+    """Scales [len(rows), K/32] of expert-sorted rows from the token-tile
+    scale arrays of stage `which` ("x": xsf / xsf_big, "i": isf / isf_big).
+    An expert with more than big_rows rows has its rows in the big tiles
+    (tile_start_big), the others in the small tiles (tile_start)."""
     L = views_np["layout"]
     seg = views_np["seg_start"]
-    ts = views_np["tile_start"]
+    counts = views_np["counts"]
+    # searchsorted(side=right) - 1 gives the last expert starting <= row: the
+    # non-empty one containing it when empty experts share its start
     e = np.searchsorted(seg, rows, side="right") - 1
-    # skip empty experts sharing a start: searchsorted(side=right)-1 gives the last expert starting <= row,
-    # which is the non-empty one containing it
     local = rows - seg[e]
-    tile = ts[e] + local // L.tile_rows
-    lr = local % L.tile_rows
+    big = (counts[e] > L.big_rows) if L.tile_rows_big > 0 else np.zeros(len(rows), bool)
     g = np.arange(K // 32)
-    off = tile_sf_offsets(tile[:, None], lr[:, None], g[None, :], L.tile_rows, K // 128)
-    return sf_bytes[off]
+    out = np.zeros((len(rows), K // 32), np.uint8)
+    for is_big, bn, ts, sf in ((False, L.tile_rows, views_np["tile_start"], views_np[which + "sf"]),
+                               (True, L.tile_rows_big, views_np["tile_start_big"], views_np[which + "sf_big"])):
+        m = big == is_big
+        if not m.any():
+            continue
+        tile = ts[e[m]] + local[m] // bn
+        lr = local[m] % bn
+        off = tile_sf_offsets(tile[:, None], lr[:, None], g[None, :], bn, K // 128)
+        out[m] = sf[off]
+    return out
 
 
 def stage_numpy(p, ws):

@@ -35,13 +35,16 @@ def test_status_strings_and_workspace(K):
         assert K.kmoe_status_string(s)
     p = K.make_params(8192, 7168, 3584, 896, 16)
     L = K.kmoe_workspace_layout(p)
-    assert L.tile_rows == 224 and L.total == K.kmoe_workspace_size(p)
+    assert (L.tile_rows, L.tile_rows_big, L.big_rows) == (64, 224, 64) and L.total == K.kmoe_workspace_size(p)
     offs = [L.err, L.topk_ids, L.topk_w, L.counts, L.seg_start, L.tile_start, L.row_of_slot, L.slot_of_row,
             L.xq, L.xsf, L.iq, L.isf, L.y]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert L.y + 8192 * 16 * 7168 * 4 <= L.total
-    assert K.kmoe_workspace_layout(K.make_params(16, 7168, 3584, 896, 16)).tile_rows == 32
-    assert K.kmoe_workspace_layout(K.make_params(128, 7168, 3584, 64, 16)).tile_rows == 64
+    for args, rows in (((16, 7168, 3584, 896, 16), (32, 0)), ((128, 7168, 3584, 64, 16), (64, 224)),
+                       ((64, 7168, 3584, 64, 16), (32, 0))):
+        Ld = K.kmoe_workspace_layout(K.make_params(*args))
+        assert (Ld.tile_rows, Ld.tile_rows_big) == rows
+    assert L.isf < L.tile_start_big < L.xsf_big < L.isf_big < L.total
 
 
 def test_host_side_argument_errors(K):

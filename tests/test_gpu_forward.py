@@ -63,14 +63,14 @@ def _check_stages(w, p, ws, s, ref, tokens):
     slots = np.arange(R)
     rows = ros[slots]
     assert np.array_equal(st["xq"][rows], xq_ref[slots // w.k])
-    got_sf = gather_row_scales(st["xsf"], st, rows, w.H)
+    got_sf = gather_row_scales(st, "x", rows, w.H)
     assert np.array_equal(got_sf, xs_ref[slots // w.k])
     # intermediate codes of the sampled tokens (masked slots excluded)
     tsl = np.array([t * w.k + j for t in tokens for j in range(w.k)])
     tsl = tsl[ids_ref.ravel()[tsl] >= 0]
     iq_gpu = st["iq"][ros[tsl]]
     iq_ref = ref["inter_q"].reshape(-1, w.I)[ids_ref[tokens].ravel() >= 0]
-    isf_gpu = gather_row_scales(st["isf"], st, ros[tsl], w.I)
+    isf_gpu = gather_row_scales(st, "i", ros[tsl], w.I)
     isf_ref = ref["inter_s"].reshape(-1, w.I // 32)[ids_ref[tokens].ravel() >= 0]
     check_intermediate_agreement(w.name, iq_gpu, iq_ref, isf_gpu, isf_ref)
     return st
@@ -121,12 +121,15 @@ def test_forward_tiny_full(K, wl):
 @pytest.mark.parametrize("wl", [PAIR_EVEN, PAIR_SKEW, PAIR_BETA, PAIR_SWIGLU], ids=["even", "skewed", "beta3", "swiglu"])
 def test_forward_pair_tiles_every_token(K, wl):
     out, ws, p, s, _ = run_forward(wl)
-    assert K.kmoe_workspace_layout(p).tile_rows == 224
+    L = K.kmoe_workspace_layout(p)
+    assert L.tile_rows_big == 224
     tokens = np.arange(wl.T)
     ref = oracle_forward(wl, s, tokens)
     st = _check_stages(wl, p, ws, s, ref, tokens)
     counts = st["counts"]
-    assert counts.max() > 224 and (counts % 224 != 0).any()  # multi-tile experts and partial tiles
+    big = counts > L.big_rows
+    # multi-tile experts and partial tiles in the 224-row (CTA-pair) class
+    assert counts.max() > 224 and (counts[big] % 224 != 0).any()
     assert_output_parity(out, ref["out"], wl.name)
 
 
@@ -141,10 +144,12 @@ def test_forward_full_size_tile_positions(K, name):
     w = W.WORKLOADS[name]
     out, ws, p, s, _ = run_forward(w)
     ids, tw, _ = O.route(s["logits"], s["bias"], w.k)
-    BN = K.kmoe_workspace_layout(p).tile_rows
-    tokens, experts = tile_position_tokens(ids, w.E, BN, n=32, seed=123)
+    L = K.kmoe_workspace_layout(p)
+    tokens, experts = tile_position_tokens(ids, w.E, L.tile_rows, n=32, seed=123, big_rows=L.big_rows,
+                                           BN_big=L.tile_rows_big)
     counts = np.bincount(ids.ravel(), minlength=w.E)
-    print(f"{name}: {len(tokens)} tokens, tile rows {BN}, experts {experts} with rows {counts[experts].tolist()}")
+    print(f"{name}: {len(tokens)} tokens, tile rows {L.tile_rows} / {L.tile_rows_big} (experts with more than "
+          f"{L.big_rows} rows), experts {experts} with rows {counts[experts].tolist()}")
     assert len(tokens) >= min(32, w.T)
     ref = oracle_forward_pool(w, s, tokens, ids, tw)
     _check_stages(w, p, ws, s, ref, tokens)
@@ -189,7 +194,7 @@ def test_forward_expert_parallel_local_slice(K):
     wl = g.with_(name="ep_local", E=e_loc)
     out, ws, p, _, _ = run_forward(wl, small=s, topk_ids=torch.from_numpy(ids).cuda(),
                                    topk_w=torch.from_numpy(wts.astype(np.float32)).cuda())
-    assert K.kmoe_workspace_layout(p).tile_rows == 224
+    assert K.kmoe_workspace_layout(p).tile_rows_big == 224
     o = out.float().cpu().numpy()
     none_local = np.all(ids < 0, axis=1)
     assert none_local.any() and np.all(o[none_local] == 0.0)
@@ -213,7 +218,7 @@ def test_determinism_and_graph_replay(K, name):
         inp, s = device_inputs(w)
         p = params(w)
         if name in ("pair_tiles", "prefill"):
-            assert K.kmoe_workspace_layout(p).tile_rows == 224
+            assert K.kmoe_workspace_layout(p).tile_rows_big == 224
         ws = torch.empty(K.kmoe_workspace_size(p), dtype=torch.uint8, device="cuda")
         outs = []
         for _ in range(3):

@@ -66,7 +66,7 @@ def test_forward_nonfinite_and_extreme_tokens(K, name):
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16)), "not bitwise deterministic"
     assert torch.isfinite(outs[0].float()).all(), "non-finite output"
     if name == "pair_tiles":
-        assert K.kmoe_workspace_layout(p).tile_rows == 224
+        assert K.kmoe_workspace_layout(p).tile_rows_big == 224
 
     st = stage_numpy(p, ws)
     # every row: payload finite, no 0xFF scale (x and intermediate)
