@@ -81,6 +81,9 @@ constexpr int kShortKBlocks = 32;
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __grid_constant__ GemmMaps maps,
                                                                      const GemmArgs a) {
+  // no tiles of this launch's class: leave before any set-up (every CTA of
+  // the cluster reads the same count)
+  if (__ldg(a.tile_start + a.E) == 0) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
