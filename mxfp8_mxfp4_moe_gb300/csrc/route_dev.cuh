@@ -210,138 +210,4 @@ __device__ __forceinline__ void route_token(const float* lg, const float* bias, 
   __syncwarp();
 }
 
-// ---------------------------------------------------------------- groups of warps
-// Routing of one token by a group of G warps, for batches too small to fill
-// the GPU with one warp per token (there the routing of a token is one warp's
-// latency chain).  Warp w of the group takes the 32-expert blocks w, w+G,
-// w+2G, ... (KPL blocks, every lane holding an expert of each block but the
-// last) and selects its own top k by exact key as route_token does; the
-// union of the G local top-k sets holds the token's top k.  Each warp writes
-// its local top k in rank order (exact key, expert id, sigmoid score; padded
-// with -inf / INT_MAX) to its list in shared memory.  After a barrier of the
-// group, one warp merges the G sorted lists (group_merge_topk): the rank of an
-// entry is its position in its own list plus, for every other list, the
-// number of entries that precede it there (larger key, or equal key and
-// lower expert id), found by binary search.
-
-// Returns false (list untouched) when more than 32 of the warp's experts stay
-// within the margin of its k-th largest cheap key even after the exact radix
-// select (many equal keys): the caller then routes the token with route_token.
-template <int KPL>
-__device__ __forceinline__ bool group_local_topk(const float* lg, const float* bias, int E, int k, int lane, int w,
-                                                 int G, float* lk, int* li, float* ls, int* s_idx) {
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  uint32_t okey[KPL];
-  uint32_t lmax = 0;
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int e = 32 * (w + G * i) + lane;
-    okey[i] = 0u;
-    if (e < E) {
-      const float kf = __fdividef(1.f, 1.f + __expf(-lg[e])) + bias[e];
-      okey[i] = order_key(isnan(kf) ? NEG_INF : kf);
-    }
-    lmax = okey[i] > lmax ? okey[i] : lmax;
-  }
-  for (int pass = 0; pass < 2; ++pass) {
-    uint32_t ocut;
-    if (pass == 0) {
-      // the k-th largest lane maximum bounds the warp's k-th largest cheap key from below
-      int rank = 0;
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t o = __shfl_sync(0xffffffffu, lmax, j);
-        rank += (o > lmax || (o == lmax && j < lane)) ? 1 : 0;
-      }
-      const unsigned who = __ballot_sync(0xffffffffu, rank == k - 1);
-      ocut = candidate_cut(order_key_inverse(__shfl_sync(0xffffffffu, lmax, __ffs(who) - 1)));
-    } else {
-      // the warp's exact k-th largest cheap key by a bitwise radix select
-      uint32_t prefix = 0;
-      for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t probe = prefix | (1u << bit);
-        unsigned cnt = 0;
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) cnt += okey[i] >= probe;
-        if (static_cast<int>(__reduce_add_sync(0xffffffffu, cnt)) >= k) prefix = probe;
-      }
-      ocut = candidate_cut(order_key_inverse(prefix));
-    }
-    int base = 0;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      const int e = 32 * (w + G * i) + lane;
-      const bool pred = e < E && okey[i] >= ocut;
-      const unsigned m = __ballot_sync(0xffffffffu, pred);
-      const int pos = base + __popc(m & ((1u << lane) - 1u));
-      if (pred && pos < 32) s_idx[pos] = e;
-      base += __popc(m);
-    }
-    __syncwarp();
-    if (base > 32) {
-      __syncwarp();
-      continue;
-    }
-    const bool have = lane < base;
-    const int idx = have ? s_idx[lane] : 0x7fffffff;
-    float sv = 0.f;
-    const float kx = have ? exact_key(lg, bias, idx, sv) : NEG_INF;
-    int rank = 0;
-    for (int j = 0; j < 32; ++j) {
-      const float kj = __shfl_sync(0xffffffffu, kx, j);
-      const int ij = __shfl_sync(0xffffffffu, idx, j);
-      rank += (kj > kx || (kj == kx && ij < idx)) ? 1 : 0;
-    }
-    // entries 0..k-1 of the list: the ranked candidates, then padding
-    if (rank < k) {
-      lk[rank] = kx;
-      li[rank] = idx;
-      ls[rank] = sv;
-    }
-    __syncwarp();
-    return true;
-  }
-  return false;
-}
-
-// Merge of the G local lists (list q at lk/li/ls + q*k), by one warp: writes
-// the token's k ids in descending key order and their renormalised weights.
-__device__ __forceinline__ void group_merge_topk(const float* lk, const int* li, const float* ls, int G, int k,
-                                                 int lane, int32_t* ids_row, float* wts_row) {
-  double sum = 0.0;
-  int my_rank[4];
-  float my_s[4];
-  int my_id[4];
-  int n = 0;
-  for (int t = lane; t < G * k; t += 32, ++n) {
-    const int q = t / k, p = t - q * k;
-    const float key = lk[t];
-    const int id = li[t];
-    int rank = p;
-    for (int q2 = 0; q2 < G; ++q2) {
-      if (q2 == q) continue;
-      // entries of list q2 preceding (key, id): a prefix of the sorted list
-      int lo = 0, hi = k;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        const float km = lk[q2 * k + mid];
-        const int im = li[q2 * k + mid];
-        if (km > key || (km == key && im < id)) lo = mid + 1; else hi = mid;
-      }
-      rank += lo;
-    }
-    my_rank[n] = rank;
-    my_s[n] = ls[t];
-    my_id[n] = id;
-    if (rank < k) sum += static_cast<double>(ls[t]);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  for (int j = 0; j < n; ++j) {
-    if (my_rank[j] < k) {
-      ids_row[my_rank[j]] = my_id[j];
-      wts_row[my_rank[j]] = static_cast<float>(static_cast<double>(my_s[j]) / sum);
-    }
-  }
-}
-
 }  // namespace kmoe
