@@ -37,7 +37,16 @@ import workloads as W  # noqa: E402
 METRIC = "Kimi-K3 MoE layer tokens/s & TFLOP/s at T=8192; µs/layer at T=16 (1×GB300)"
 HEADLINE = "prefill"     # T=8192 layer
 DECODE = "decode"        # T=16 layer
-KERNEL_LAUNCHES_PER_STEP = 7  # route, rank, scan, quantise-scatter, FC1, FC2, combine
+BIG_TILE_ROWS_ABOVE = 64  # experts with more rows than this take the 224-row CTA-pair tiles
+
+
+def kernel_launches(w) -> int:
+    """Kernels of this library one forward launches: routing; the permutation
+    (rank + scan, or one block when R <= 1024); quantise-scatter; FC1 and FC2
+    (each a CTA-pair launch for the big-tile experts, left out when no expert
+    can exceed 64 rows (T <= 64), and a small-tile launch); combine."""
+    fc = 2 if w.T > BIG_TILE_ROWS_ABOVE else 1
+    return 1 + (2 if w.R > 1024 else 1) + 1 + 2 * fc + 1
 ROUNDS = 5               # interleaved timing rounds (median reported)
 # the five seeded workloads, timed in turn within every round; the small ones
 # (inputs that fit in L2) with the L2 flushed before every timed forward
@@ -676,11 +685,8 @@ def run_ours(args):
             "rounds_ms": rounds[n], "forwards_per_round": [c for c in counts[n] if c],
             "timing": ("each forward timed alone after a write of 2 x L2 (inputs fit in L2)" if n in FLUSHED
                        else "back-to-back forwards (weights larger than L2)")}
-    # kernels of this library launched in the timed region: 7 per forward
-    # (route, rank, scan, quantise-scatter, FC1, FC2, combine), 6 when the
-    # layer has at most 1024 routed slots (the permutation runs in one block)
-    gpu_launches = sum(sum(counts[n]) * (KERNEL_LAUNCHES_PER_STEP if W.WORKLOADS[n].R > 1024
-                                         else KERNEL_LAUNCHES_PER_STEP - 1) for n in layers)
+    # kernels of this library launched in the timed region (kernel_launches per forward)
+    gpu_launches = sum(sum(counts[n]) * kernel_launches(W.WORKLOADS[n]) for n in layers)
     stages = time_stages(layer, max(3, min(args.steps, 10)))
     layer.check()
     fc1_ms = stages[3]

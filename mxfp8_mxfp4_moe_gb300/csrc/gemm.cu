@@ -140,7 +140,9 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
     // ------------------------------------------------------------ producers
     // warp 0: weight codes and scales; warp PRODB_WARP: token rows and their
     // scales.  Both arrive on the stage's full barrier with their own bytes.
-    if (lane == 0) {
+    // The whole warp runs the loop converged and one elected lane issues each
+    // copy and arrival (ptx.cuh, the _el forms).
+    {
       const bool is_a = warp == 0;
       const uint64_t pol = is_a ? policy_evict_normal() : policy_evict_last();
       uint32_t it = 0;
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
 #pragma unroll
               for (int j = 0; j < C::NT; ++j) {
                 const size_t blk = static_cast<size_t>(pblk0 + j * a.KB);
-                bulk_prefetch_l2(a.wq + blk * 8192, C::KPS * 8192);
-                bulk_prefetch_l2(a.wsf + blk * 512, C::KPS * 512);
+                bulk_prefetch_l2_el(a.wq + blk * 8192, C::KPS * 8192);
+                bulk_prefetch_l2_el(a.wsf + blk * 512, C::KPS * 512);
               }
               ++pit;
               pkb += C::KPS;
@@ -179,18 +181,18 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
               }
             }
           }
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + s * C::STAGE;
-          mbar_arrive_expect_tx(&full[s], tx);
+          mbar_arrive_expect_tx_el(&full[s], tx);
           if (is_a) {
 #pragma unroll
             for (int j = 0; j < C::NT; ++j) {
               const int blk = blk0 + j * a.KB + kb;
-              tma_load_3d(st + j * C::KPS * C::A_KB, &maps.a, &full[s], 0, 0, blk, pol);
-              bulk_load(st + C::SFA_OFF + j * C::KPS * 512, a.wsf + static_cast<size_t>(blk) * 512, C::KPS * 512,
+              tma_load_3d_el(st + j * C::KPS * C::A_KB, &maps.a, &full[s], 0, 0, blk, pol);
+              bulk_load_el(st + C::SFA_OFF + j * C::KPS * 512, a.wsf + static_cast<size_t>(blk) * 512, C::KPS * 512,
                         &full[s]);
             }
           } else {
@@ -199,19 +201,19 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
               uint8_t* sb = st + C::B_OFF + kbi * C::B_KB;
               const int x = (kb + kbi) * 128;
               if (ng == C::BN / 32) {
-                tma_load_2d(sb, &maps.b[3], &full[s], x, wk.r0, pol);  // a whole tile in one box
+                tma_load_2d_el(sb, &maps.b[3], &full[s], x, wk.r0, pol);  // a whole tile in one box
               } else {
                 int g = 0;  // the tile's token rows in boxes of 128, 64 and 32 rows
                 for (int lv = 2; lv >= 0; --lv) {
                   const int rows_g = 1 << lv;
                   while (ng - g >= rows_g) {
-                    tma_load_2d(sb + g * 4096, &maps.b[lv], &full[s], x, wk.r0 + 32 * g, pol);
+                    tma_load_2d_el(sb + g * 4096, &maps.b[lv], &full[s], x, wk.r0 + 32 * g, pol);
                     g += rows_g;
                   }
                 }
               }
             }
-            bulk_load(st + C::SFB_OFF, bsf + static_cast<size_t>(kb) * C::NCH * 512, C::KPS * C::NCH * 512,
+            bulk_load_el(st + C::SFB_OFF, bsf + static_cast<size_t>(kb) * C::NCH * 512, C::KPS * C::NCH * 512,
                       &full[s]);
           }
         }
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(co
         // let the copies already issued land before the CTA can exit
         const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
         for (uint32_t i = first; i < it; ++i)
-          mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1u, 20000000ull, nullptr, nullptr);
+          mbar_wait_warp(&full[i % C::STAGES], (i / C::STAGES) & 1u, 20000000ull, nullptr, nullptr);
       }
     }
   } else if (warp == 1) {

@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
   // With DYN off the pair takes items p, p + npairs, ... (no ring).
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
-  const bool fetcher = C::DYN && lead && warp == C::PRODB_WARP && lane == 0;
+  const bool fetcher = C::DYN && lead && warp == C::PRODB_WARP;  // the whole warp; lane 0 claims and publishes
   auto get_item = [&](uint32_t li) -> int {
     if (!C::DYN) {
       const int w = pair + static_cast<int>(li) * npairs;
@@ -170,50 +170,62 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
 
   if (warp == 0 || warp == C::PRODB_WARP) {
     // ------------------------------------------------------------ producers
-    // Both CTAs' loads complete on the even CTA's full barrier (the TMA
-    // .cta_group::2 form); its producers expect the bytes of both CTAs.
-    if (lane == 0) {
+    // The whole warp runs the loop converged and one elected lane issues each
+    // copy and arrival (ptx.cuh, the _el forms).  Both CTAs' loads complete on
+    // the even CTA's full barrier (the TMA .cta_group::2 form); its producers
+    // expect the bytes of both CTAs.
+    {
       const bool is_a = warp == 0;
       const uint64_t pol = is_a ? policy_evict_normal() : policy_evict_last();
       const uint32_t tx2 = 2u * C::KPS * (is_a ? C::A_TX + 512 : C::B_BYTES + C::NCH * 512);
       const uint32_t lead_full = cluster_map(full, 0);
       uint32_t it = 0;
       bool ok = true;
-      // the fetcher's publication state; each claim (atomicAdd) is issued one
-      // item before its value is needed, so its latency overlaps the loads
+      // the fetcher's publication state (the same in every lane); each claim
+      // (atomicAdd, lane 0) is issued one item before its value is needed, so
+      // its latency overlaps the loads
       uint32_t published = 0;
       bool ended = false;
-      int claimed = 0;
+      int claimed = 0;  // lane 0's
       const uint32_t peer_item_full = cluster_map(item_full, 1);
       const uint32_t peer_item_w = cluster_map(const_cast<int*>(item_w), 1);
-      auto publish = [&](int w) {
+      auto publish = [&](int w_lane0) {
+        int w = __shfl_sync(0xffffffffu, w_lane0, 0);
         if (ended) return;
         if (w >= total) {
           w = -1;
           ended = true;
         }
         const uint32_t sl = published % kRing;
-        item_w[sl] = w;
-        st_shared_cluster_u32(peer_item_w + 4u * sl, static_cast<uint32_t>(w));
-        mbar_arrive(&item_full[sl]);                    // release: orders the local store
-        mbar_arrive_remote(peer_item_full + 8u * sl);   // release.cluster: orders the remote store
+        if (lane == 0) {
+          item_w[sl] = w;
+          st_shared_cluster_u32(peer_item_w + 4u * sl, static_cast<uint32_t>(w));
+          mbar_arrive(&item_full[sl]);                    // release: orders the local store
+          mbar_arrive_remote(peer_item_full + 8u * sl);   // release.cluster: orders the remote store
+        }
+        __syncwarp();
         ++published;
       };
       if (fetcher) {
-        publish(atomicAdd(a.sched, 1));
-        publish(atomicAdd(a.sched, 1));
-        claimed = atomicAdd(a.sched, 1);
+        int c0 = 0, c1 = 0;
+        if (lane == 0) {
+          c0 = atomicAdd(a.sched, 1);
+          c1 = atomicAdd(a.sched, 1);
+          claimed = atomicAdd(a.sched, 1);
+        }
+        publish(c0);
+        publish(c1);
       }
       for (uint32_t li = 0; ok; ++li) {
         int w;
         if (fetcher) {
-          w = item_w[li % kRing];  // published by this thread
+          w = item_w[li % kRing];  // published by this warp
           if (w >= 0 && !ended) {
             publish(claimed);      // keep two items published ahead
-            if (!ended) claimed = atomicAdd(a.sched, 1);
+            if (!ended && lane == 0) claimed = atomicAdd(a.sched, 1);
           }
         } else {
-          w = get_item(li);
+          w = get_item_warp(li);
         }
         if (w < 0) break;
         Work wk;
@@ -226,27 +238,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
         for (int kb = 0; kb < a.KB; kb += C::KPS, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + s * C::STAGE;
           const uint32_t bar = lead_full + 8u * s;
           if (lead) {
-            if (!is_a && kb == 0) item_n[li & 3u] = nmma;
-            mbar_arrive_expect_tx(&full[s], tx2);
+            if (!is_a && kb == 0) item_n[li & 3u] = nmma;  // every lane stores the same value
+            mbar_arrive_expect_tx_el(&full[s], tx2);
           }
 #pragma unroll
           for (int kbi = 0; kbi < C::KPS; ++kbi) {
             if (is_a) {
-              tma_load_3d_pair(st + kbi * C::A_KB, &maps.a, bar, 0, 0, blk0 + kb + kbi, pol);
-              tma_load_2d_pair(st + C::SFA_OFF + kbi * 512, &maps.asf, bar, 0, 4 * (blk0 + kb + kbi), pol);
+              tma_load_3d_pair_el(st + kbi * C::A_KB, &maps.a, bar, 0, 0, blk0 + kb + kbi, pol);
+              tma_load_2d_pair_el(st + C::SFA_OFF + kbi * 512, &maps.asf, bar, 0, 4 * (blk0 + kb + kbi), pol);
             } else {
               // this CTA's half of the MMA's token rows (rows past the tile are
               // loaded but not used; rows past the tensor read as zero)
-              tma_load_2d_pair(st + C::B_OFF + kbi * C::B_BYTES, &maps.b[4], bar, (kb + kbi) * 128, brow, pol);
-              tma_load_2d_pair(st + C::SFB_OFF + kbi * C::NCH * 512, &maps.bsf, bar, 0,
-                               sfrow0 + (kb + kbi) * C::NCH * 4, pol);
+              tma_load_2d_pair_el(st + C::B_OFF + kbi * C::B_BYTES, &maps.b[4], bar, (kb + kbi) * 128, brow, pol);
+              tma_load_2d_pair_el(st + C::SFB_OFF + kbi * C::NCH * 512, &maps.bsf, bar, 0,
+                                  sfrow0 + (kb + kbi) * C::NCH * 4, pol);
             }
           }
         }
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
         if (lead) {
           const uint32_t first = it > static_cast<uint32_t>(C::STAGES) ? it - C::STAGES : 0u;
           for (uint32_t i = first; i < it; ++i)
-            mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1u, 20000000ull, nullptr, nullptr);
+            mbar_wait_warp(&full[i % C::STAGES], (i / C::STAGES) & 1u, 20000000ull, nullptr, nullptr);
         } else {
           spin_ns(100000ull);
         }
