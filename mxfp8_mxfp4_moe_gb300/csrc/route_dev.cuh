@@ -73,6 +73,31 @@ __device__ __forceinline__ uint32_t candidate_cut(float kth) {
   return order_key((kth == NEG_INF) ? NEG_INF : kth - margin);
 }
 
+// Bitonic sort of one value per lane across the warp into descending order
+// (lane 0 the largest): 15 compare-exchange steps of one shuffle each, in
+// place of 32 rounds of broadcast-and-count.  `before(a, i, b, j)` says
+// whether (a, i) precedes (b, j); the payload p travels with its key.
+template <class K, class Before>
+__device__ __forceinline__ void warp_sort_desc(K& key, int& idx, float& p, int lane, Before before) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const K ok = __shfl_xor_sync(0xffffffffu, key, stride);
+      const int oi = __shfl_xor_sync(0xffffffffu, idx, stride);
+      const float op = __shfl_xor_sync(0xffffffffu, p, stride);
+      const bool lower = (lane & stride) == 0;   // lower lane of the pair
+      const bool desc = (lane & size) == 0;      // this block sorts descending
+      const bool mine_first = before(key, idx, ok, oi);
+      if (mine_first != (lower == desc)) {
+        key = ok;
+        idx = oi;
+        p = op;
+      }
+    }
+  }
+}
+
 // Candidates (order key >= ocut) one per lane, ranked by exact key across the
 // warp; writes the top k and returns true, or returns false (nothing written)
 // when there are more than 32 candidates.
@@ -97,22 +122,19 @@ __device__ __forceinline__ bool select_ranked(const uint32_t (&okey)[KPL], uint3
     return false;
   }
   const bool have = lane < base;
-  const int idx = have ? s_idx[lane] : 0x7fffffff;
+  int idx = have ? s_idx[lane] : 0x7fffffff;
   float sv = 0.f;
-  const float kx = have ? exact_key(lg, bias, idx, sv) : NEG_INF;
-  int rank = 0;
-  for (int j = 0; j < 32; ++j) {
-    const float kj = __shfl_sync(0xffffffffu, kx, j);
-    const int ij = __shfl_sync(0xffffffffu, idx, j);
-    rank += (kj > kx || (kj == kx && ij < idx)) ? 1 : 0;
-  }
-  const bool sel = have && rank < k;
+  float kx = have ? exact_key(lg, bias, idx, sv) : NEG_INF;
+  // sorted by exact key (equal keys: lower expert id first); lane r holds rank r
+  warp_sort_desc(kx, idx, sv, lane,
+                 [](float a, int i, float b, int j) { return a > b || (a == b && i < j); });
+  const bool sel = lane < k;  // base >= k: every rank below k is a candidate
   double sum = sel ? static_cast<double>(sv) : 0.0;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   if (sel) {
-    ids_row[rank] = idx;
-    wts_row[rank] = static_cast<float>(static_cast<double>(sv) / sum);
+    ids_row[lane] = idx;
+    wts_row[lane] = __fdiv_rn(sv, static_cast<float>(sum));
   }
   __syncwarp();  // s_idx is reused by this warp's next token
   return true;
@@ -148,13 +170,11 @@ __device__ __forceinline__ void route_token(const float* lg, const float* bias, 
   // 1. the k-th largest lane maximum (ranks 0..31, ties by lane) bounds the
   //    k-th largest cheap key from below
   {
-    int rank = 0;
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t o = __shfl_sync(0xffffffffu, lmax, j);
-      rank += (o > lmax || (o == lmax && j < lane)) ? 1 : 0;
-    }
-    const unsigned who = __ballot_sync(0xffffffffu, rank == k - 1);
-    const float lb = order_key_inverse(__shfl_sync(0xffffffffu, lmax, __ffs(who) - 1));
+    uint32_t sk = lmax;
+    int sl = lane;
+    float unused = 0.f;
+    warp_sort_desc(sk, sl, unused, lane, [](uint32_t a, int i, uint32_t b, int j) { return a > b || (a == b && i < j); });
+    const float lb = order_key_inverse(__shfl_sync(0xffffffffu, sk, k - 1));
     if (select_ranked<KPL>(okey, candidate_cut(lb), lg, bias, E, k, lane, ids_row, wts_row, s_idx)) return;
   }
   // 2. the exact k-th largest cheap key, by a bitwise radix select over the

@@ -38,9 +38,9 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kFirstRouteWarp = 6;
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 24;
 constexpr int kATile = 128 * 128;        // 128 tokens x 64 bf16 (the MMA's M = 128 rows)
-constexpr int kStageArea = 192 * 1024;   // stages of kATile + EN x 128 bytes, 1 KB aligned
+constexpr int kStageArea = 192 * 1024;   // stages of the x tile + EN x 128 bytes, 1 KB aligned
 constexpr int kStgOff = kStageArea;      // epilogue staging: 32 x 32 fp32 per warp
 constexpr int kBarOff = kStgOff + 4 * 4096;
 constexpr int kBiasOff = kBarOff + 512;
@@ -175,7 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < a.E; e += kThreads) s_b[e] = a.bias[e];
   const int EN = a.plan.EN, nch = a.plan.nch, items = a.plan.items, S = a.plan.S, kper = a.plan.kper;
-  const int stride = (kATile + EN * 128 + 1023) & ~1023;  // bytes per pipeline stage
+  // a stage holds the x tile (xrows of the MMA's 128 A rows: the MMA reads
+  // past it into the rest of shared memory for the rows >= T, whose
+  // accumulator lanes are never stored) and the EN-expert gate tile; small
+  // batches thus fit more stages in flight
+  const int atile = a.xrows * 128;
+  const int stride = (atile + EN * 128 + 1023) & ~1023;  // bytes per pipeline stage
   const int nst = kStageArea / stride < kMaxStages ? kStageArea / stride : kMaxStages;
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
           uint8_t* st = smem + s * stride;
           mbar_arrive_expect_tx(&full[s], tx);
           tma_load_2d(st, &maps.x, &full[s], 64 * ks, 128 * mt, pol_x);
-          tma_load_2d(st + kATile, &maps.g, &full[s], 64 * ks, EN * nc, pol_g);
+          tma_load_2d(st + atile, &maps.g, &full[s], 64 * ks, EN * nc, pol_g);
         }
       }
       if (!ok) {
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
     {
       const uint32_t idesc = idesc_bf16(128, static_cast<uint32_t>(EN));
       const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(smem));
-      const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + kATile));
+      const uint64_t bdesc0 = sdesc_kmajor_sw128(smem_u32(smem + atile));
       int s = 0;
       uint32_t ph = 0, li = 0;
       bool ok = true;
