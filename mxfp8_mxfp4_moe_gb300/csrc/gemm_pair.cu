@@ -32,6 +32,10 @@ struct PairCfg {
   static constexpr int STAGES = STAGES_;
   static constexpr bool DYN = DYN_;  // work items claimed dynamically (else pair p takes p, p + npairs, ...)
   static constexpr int UV = UV_;     // FC1 activation values per epilogue work unit (8 or 16)
+  // the short-K instantiation (8-value units): all four warps of an epilogue
+  // group do activation math, the one on the MMA warp's scheduler included
+  // (the epilogue is the limit there; at long K that warp only stages)
+  static constexpr bool SHORT_K = UV_ == 8;
   static constexpr int KPS = 2;          // 128-wide K blocks per stage (8 pair MMAs)
   static constexpr int BN = 224;         // token rows per item (both CTAs)
   static constexpr int HALF = BN / 2;    // token rows loaded by each CTA
@@ -73,9 +77,10 @@ struct PairCfg {
 constexpr int kRing = 8;  // work-item ring slots
 // FC1 with at most this many 128-wide K blocks (H = 3584: 28) has a main loop
 // short enough that the epilogue is on the critical path: its kernel uses
-// 8-value activation units, which spread the SiTU work more evenly over the
-// three math warps (FC1 3.54 -> 3.25 ms at H = 3584, I = 3072, T = 8192; at
-// H = 7168 the 16-value units are faster).
+// 8-value activation units on all four warps of an epilogue group (FC1 3.54
+// -> 3.25 ms at H = 3584, I = 3072, T = 8192 with 8-value units on three
+// warps, 3.00 -> 2.87 ms on four once the MMA warp issued converged; at
+// H = 7168 16-value units on three warps are faster).
 constexpr int kShortKBlocks = 32;
 
 template <class C>
@@ -346,9 +351,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
     const int eq = ew & 3;
     // Warp w runs on scheduler w % 4: the MMA warp (1) shares one with the
     // epilogue warp of lane quarter 1, the token producer (PRODB_WARP) with
-    // quarter 2's.  The quarter-1 warp leaves the SiTU math to the other
-    // three, and the extra pass goes to the warp whose scheduler hosts no
-    // other role.
+    // quarter 2's.  At long K the quarter-1 warp leaves the activation math
+    // to the other three, and the extra pass goes to the warp whose
+    // scheduler hosts no other role; at short K all four do math.
     constexpr int kMmaSchedEq = (1 + 4 - 2) & 3;
     constexpr int kHeavyEq = 1;  // warp 3, scheduler 3
     static_assert(((kHeavyEq + 2) & 3) != (C::PRODB_WARP & 3) && ((kHeavyEq + 2) & 3) != 0 &&
@@ -371,8 +376,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
       const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * C::BN;
       const int nchunk = (wk.n + 31) >> 5;
       for (int ci = grp; ci < nchunk; ci += C::NGRP)
-        epilogue_chunk<C::FC1, C::NCH, C::UV>(a, wk, mt, tacc, ci * 32, stg, q, eq, lane, grp, kMmaSchedEq,
-                                              kHeavyEq);
+        epilogue_chunk<C::FC1, C::NCH, C::UV>(a, wk, mt, tacc, ci * 32, stg, q, eq, lane, grp,
+                                              C::SHORT_K ? -1 : kMmaSchedEq, C::SHORT_K ? -1 : kHeavyEq);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
