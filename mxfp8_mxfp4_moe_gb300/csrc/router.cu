@@ -114,10 +114,20 @@ __device__ __forceinline__ void store_logit_tile(uint32_t tacc, int EN, float* s
   }
 }
 
+// The bias is read by the routing warps after the set-up, off the path of
+// the GEMM roles (a cold read takes over a microsecond); each thread arrives
+// on bias_bar after its stores, and every warp waits on it before routing.
+__device__ __forceinline__ void load_bias(const RouterArgs& a, float* s_b, uint64_t* bias_bar, int warp) {
+  if (warp < kFirstRouteWarp) return;
+  for (int e = threadIdx.x - 32 * kFirstRouteWarp; e < a.E; e += 32 * (kWarps - kFirstRouteWarp)) s_b[e] = a.bias[e];
+  mbar_arrive(bias_bar);
+}
+
 // Routing warps: tokens are handed out in increasing order, so the first
 // tiles' tokens are routed while later tiles are still in the GEMM.
 template <int KPL>
-__device__ void route_pool(const RouterArgs& a, const float* s_b, int* s_idx, int lane) {
+__device__ void route_pool(const RouterArgs& a, const float* s_b, uint64_t* bias_bar, int* s_idx, int lane) {
+  if (!mbar_wait_warp(bias_bar, 0, a.budget_ns, a.err, nullptr)) return;
   int* next = a.sync;
   const int* tile_done = a.sync + 2;
   const int need = a.plan.nch;  // one count per expert chunk of the tile
@@ -165,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
   uint64_t* acc_full = empty + kMaxStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* bias_bar = done + 1;  // the routing warps' copy of the bias is in s_b
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bias_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // epilogue: last split
   float* s_b = reinterpret_cast<float*>(smem + kBiasOff);
@@ -173,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  for (int e = threadIdx.x; e < a.E; e += kThreads) s_b[e] = a.bias[e];
   const int EN = a.plan.EN, nch = a.plan.nch, items = a.plan.items, S = a.plan.S, kper = a.plan.kper;
   // a stage holds the x tile (xrows of the MMA's 128 A rows: the MMA reads
   // past it into the rest of shared memory for the rows >= T, whose
@@ -192,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
       mbar_init(&acc_empty[b], 4);
     }
     mbar_init(done, 1);
+    mbar_init(bias_bar, 32 * (kWarps - kFirstRouteWarp));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -207,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  load_bias(a, s_b, bias_bar, warp);
   const int KS = a.H / 64;
   const uint64_t budget = a.budget_ns;
   int* tile_done = a.sync + 2;
@@ -221,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
+    // the whole warp runs the loop converged; one elected lane issues
+    {
       const uint32_t tx = static_cast<uint32_t>(a.xrows + EN) * 128;
       const uint64_t pol_x = policy_evict_normal();
       const uint64_t pol_g = policy_evict_last();  // the gate weight is re-read by every token tile
@@ -234,21 +247,21 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
         for (int ks = sp * kper; ks < ks1; ++ks, ++n) {
           const int s = static_cast<int>(n % nst);
           const uint32_t ph = (n / nst) & 1u;
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + s * stride;
-          mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_2d(st, &maps.x, &full[s], 64 * ks, 128 * mt, pol_x);
-          tma_load_2d(st + atile, &maps.g, &full[s], 64 * ks, EN * nc, pol_g);
+          mbar_arrive_expect_tx_el(&full[s], tx);
+          tma_load_2d_el(st, &maps.x, &full[s], 64 * ks, 128 * mt, pol_x);
+          tma_load_2d_el(st + atile, &maps.g, &full[s], 64 * ks, EN * nc, pol_g);
         }
       }
       if (!ok) {
         // let the copies already issued land before the CTA can exit
         const uint32_t first = n > static_cast<uint32_t>(nst) ? n - nst : 0u;
         for (uint32_t i = first; i < n; ++i)
-          mbar_wait_bounded(&full[i % nst], (i / nst) & 1u, 20000000ull, nullptr, nullptr);
+          mbar_wait_warp(&full[i % nst], (i / nst) & 1u, 20000000ull, nullptr, nullptr);
       }
     }
     __syncwarp();
@@ -351,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_kernel(const __grid_consta
       if (warp == 2 && lane == 0) atomicAdd(tile_done + mt, 1);
     }
   }
-  route_pool<KPL>(a, s_b, s_idx + warp * 32, lane);
+  route_pool<KPL>(a, s_b, bias_bar, s_idx + warp * 32, lane);
 
   tc_fence_before();
   __syncthreads();
@@ -381,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
   uint64_t* acc_full = empty + kMaxStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* bias_bar = done + 1;  // the routing warps' copy of the bias is in s_b
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bias_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* s_b = reinterpret_cast<float*>(smem + kBiasOff);
   int* s_idx = reinterpret_cast<int*>(smem + kIdxOff);
@@ -390,7 +404,6 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool lead = rank == 0;
-  for (int e = threadIdx.x; e < a.E; e += kThreads) s_b[e] = a.bias[e];
   const int EN = a.plan.EN, nch = a.plan.nch, items = a.plan.items, tiles = a.plan.tiles;
   const int half = EN / 2;
   const int stride = (kATile + half * 128 + 1023) & ~1023;  // bytes per pipeline stage
@@ -405,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
       mbar_init(&acc_empty[b], 8);  // the epilogue warps of both CTAs
     }
     mbar_init(done, 1);
+    mbar_init(bias_bar, 32 * (kWarps - kFirstRouteWarp));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -421,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
   cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  load_bias(a, s_b, bias_bar, warp);
   const int KS = a.H / 64;
   const uint64_t budget = a.budget_ns;
   int* tile_done = a.sync + 2;
@@ -429,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producers (both CTAs)
-    if (lane == 0) {
+    // the whole warp runs the loop converged; one elected lane issues
+    {
       const uint32_t tx2 = 2u * static_cast<uint32_t>(kATile + half * 128);
       const uint64_t pol_x = policy_evict_normal();
       const uint64_t pol_g = policy_evict_last();
@@ -443,15 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
         for (int ks = 0; ks < KS; ++ks, ++n) {
           const int s = static_cast<int>(n % nst);
           const uint32_t ph = (n / nst) & 1u;
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
+          if (!mbar_wait_warp(&empty[s], ph ^ 1u, budget, a.err, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + s * stride;
           const uint32_t bar = lead_full + 8u * static_cast<uint32_t>(s);
-          if (lead) mbar_arrive_expect_tx(&full[s], tx2);
-          tma_load_2d_pair(st, &maps.x, bar, 64 * ks, 128 * mt, pol_x);
-          tma_load_2d_pair(st + kATile, &maps.g, bar, 64 * ks, grow, pol_g);
+          if (lead) mbar_arrive_expect_tx_el(&full[s], tx2);
+          tma_load_2d_pair_el(st, &maps.x, bar, 64 * ks, 128 * mt, pol_x);
+          tma_load_2d_pair_el(st + kATile, &maps.g, bar, 64 * ks, grow, pol_g);
         }
       }
       if (!ok) {
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
         if (lead) {
           const uint32_t first = n > static_cast<uint32_t>(nst) ? n - nst : 0u;
           for (uint32_t i = first; i < n; ++i)
-            mbar_wait_bounded(&full[i % nst], (i / nst) & 1u, 20000000ull, nullptr, nullptr);
+            mbar_wait_warp(&full[i % nst], (i / nst) & 1u, 20000000ull, nullptr, nullptr);
         } else {
           spin_ns(100000ull);
         }
@@ -535,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_pair_kernel(const __grid_c
       if (warp == 2 && lane == 0 && mt < tiles) atomicAdd(tile_done + mt, 1);
     }
   }
-  route_pool<KPL>(a, s_b, s_idx + warp * 32, lane);
+  route_pool<KPL>(a, s_b, bias_bar, s_idx + warp * 32, lane);
 
   tc_fence_before();
   __syncthreads();
