@@ -49,9 +49,11 @@ struct PairCfg {
   static constexpr int SFA_OFF = B_OFF + KPS * B_BYTES;
   static constexpr int SFB_OFF = SFA_OFF + KPS * 512;
   static constexpr int STAGE = (SFB_OFF + KPS * NCH * 512 + 1023) / 1024 * 1024;
-  // FC1: two groups of four (its SiTU epilogue must stay shorter than a short-K main loop);
-  // FC2: one warp per TMEM lane quarter
-  static constexpr int EPI_WARPS = FC1 ? 8 : 4;
+  // two groups of four warps (one per TMEM lane quarter) taking alternate
+  // 32-column chunks: FC1's SiTU epilogue must stay shorter than a short-K
+  // main loop, and FC2's scattered fp32 stores with one group were on the
+  // critical path (FC2 3.15 -> 2.76 ms at T=8192; 12 or 16 warps: 2.79, 2.83)
+  static constexpr int EPI_WARPS = 8;
   static constexpr int NGRP = EPI_WARPS / 4;
   static constexpr int PRODB_WARP = 2 + EPI_WARPS;
   static constexpr int THREADS = 32 * (3 + EPI_WARPS);
