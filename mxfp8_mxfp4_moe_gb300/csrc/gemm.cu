@@ -20,13 +20,17 @@
 //
 // Warp roles (persistent; one CTA per SM for the 224-row tiles, two for the
 // 32- and 64-row tiles):
-//   warp 0      TMA producer of the weight codes and scales (one lane)
-//   warp 1      TMEM owner and MMA issuer (one lane)
+//   warp 0      TMA producer of the weight codes and scales
+//   warp 1      TMEM owner and MMA issuer
 //   warps 2..   epilogue, EPI_WARPS in groups of four; warp w reads TMEM lane
 //               quarter w % 4, group g = (w - 2) / 4 takes the 32-column
 //               chunks NGRP*i + g of the tile
-//   last warp   TMA producer of the token rows and their scales (one lane)
-// Two producer warps keep more bulk copies in flight than one thread can.
+//   last warp   TMA producer of the token rows and their scales
+// The producer and MMA warps run their loops with all lanes converged; one
+// lane, elected inside each instruction sequence, issues every copy and
+// tcgen05 operation (a lone lane in a divergent branch issues them several
+// times more slowly).  Two producer warps keep more bulk copies in flight
+// than one thread can.
 // Pipelines: STAGES smem stages (full/empty mbarriers) and NACC TMEM
 // accumulator sets (acc_full/acc_empty); with two, the epilogue of one work
 // item overlaps the main loop of the next.  Every wait is bounded.

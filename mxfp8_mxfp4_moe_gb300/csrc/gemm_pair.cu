@@ -13,8 +13,8 @@
 //
 // Roles in each CTA of the pair:
 //   warp 0      TMA of the CTA's weight block and its 512 scale bytes
-//   warp 1      TMEM allocation (both CTAs); in the even CTA one lane issues
-//               the pair MMAs
+//   warp 1      TMEM allocation (both CTAs); in the even CTA it issues the
+//               pair MMAs (converged, one elected lane per instruction)
 //   warps 2..9  epilogue on the CTA's own accumulator (as in the one-CTA kernel)
 //   warp 10     TMA of the CTA's token rows (token tile rows [rN/2, rN/2+112))
 //               and of the scales of all token rows of the tile

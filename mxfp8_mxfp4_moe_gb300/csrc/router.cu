@@ -7,8 +7,10 @@
 //   warp 0        TMA producer: per K step of 64, the x tile (128 tokens, or
 //                 32 / 64 when T is that small) and the EN-expert gate tile
 //                 (both bf16, 128-byte swizzle); as many pipeline stages as
-//                 192 KB holds (4 at EN = 256 .. 9 at EN = 32), since the loop
-//                 is bound by the bytes in flight per SM
+//                 192 KB holds, up to 24 (4 at EN = 256 with 128-token x
+//                 tiles, 24 at EN = 32 with 32-token tiles), since the loop
+//                 is bound by the bytes in flight per SM; the warp runs
+//                 converged and one elected lane issues each copy
 //   warp 1        TMEM owner and MMA issuer: tcgen05.mma .kind::f16 (bf16 x
 //                 bf16 -> fp32), M = 128 tokens, N = EN experts, K = 16 per
 //                 instruction; two 256-column accumulators so that the
@@ -19,9 +21,10 @@
 //                 split S ways (few items: decode) each split writes a
 //                 partial tile and the last split of a (tile, chunk) to
 //                 finish sums the S partials in split order into the logits
-//   warps 6..15   routing: take tokens one at a time from a global counter,
-//                 wait (bounded) until every expert chunk of the token's tile
-//                 is written, route the token (route_dev.cuh)
+//   warps 6..15   routing: first copy the correction bias into shared
+//                 memory, then take tokens one at a time from a global
+//                 counter, wait (bounded) until every expert chunk of the
+//                 token's tile is written, route the token (route_dev.cuh)
 // The GEMM warps join the routing pool when their work runs out, so routing
 // of finished token tiles overlaps the gate GEMM of the rest.  Every wait is
 // bounded; a wait that gives up sets the timeout bit and the token is left
