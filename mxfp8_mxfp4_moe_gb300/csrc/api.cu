@@ -14,13 +14,13 @@
 namespace kmoe {
 cudaError_t launch_route(const float*, const float*, int, int, int, int32_t*, float*, cudaStream_t);
 cudaError_t launch_permute(const int32_t*, int, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*,
-                           int32_t*, uint32_t*, cudaStream_t);
+                           int32_t*, uint32_t*, cudaStream_t, bool);
 cudaError_t launch_quant_rows(const void*, int, int, int, uint8_t*, uint8_t*, cudaStream_t);
 cudaError_t launch_quant_scatter(const void*, int, int, int, int, int, int, const int32_t*, const int32_t*,
                                  const int32_t*, const int32_t*, const int32_t*, const int32_t*, const int32_t*,
-                                 int32_t*, int32_t*, uint8_t*, uint8_t*, uint8_t*, cudaStream_t);
+                                 int32_t*, int32_t*, uint8_t*, uint8_t*, uint8_t*, cudaStream_t, bool);
 cudaError_t launch_combine(const float*, const int32_t*, const float*, int, int, int, int, float, void*,
-                           cudaStream_t);
+                           cudaStream_t, bool);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t budget_ns, cudaStream_t st);
 cudaError_t launch_activation_selftest(const float*, const float*, int, int, float, float, float, float, float, float,
                                        float*, cudaStream_t);
@@ -376,11 +376,15 @@ static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* l
     KMOE_CK(launch_route(logits, bias, T, E, k, ids, wts, stream));
   }
   KMOE_CK(mark(ev ? ev->routed : nullptr));
+  // Kernels after the first are chained (launch_chained): each may begin
+  // launching while its predecessor runs.  Not across stage events (their
+  // records sit between the kernels), nor after the copy of given ids.
+  const bool pdl = ev == nullptr;
   KMOE_CK(launch_permute(ids, R, E, L.BN, thr, rank, chunk_prefix, counts, seg_start, tile_start, tile_start_big, err,
-                         stream));
+                         stream, pdl && !given));
   KMOE_CK(mark(ev ? ev->permuted : nullptr));
   KMOE_CK(launch_quant_scatter(x_bf16, T, H, k, E, L.BN, thr, ids, rank, chunk_prefix, counts, seg_start, tile_start,
-                               tile_start_big, row_of_slot, slot_of_row, xq, xsf, xsf_big, stream));
+                               tile_start_big, row_of_slot, slot_of_row, xq, xsf, xsf_big, stream, pdl));
   KMOE_CK(mark(ev ? ev->quantized : nullptr));
   const int grid = num_sms();
   if (grid <= 0) return KMOE_ERR_CUDA;
@@ -398,9 +402,9 @@ static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* l
     ab1.bsf = xsf_big;
     ab1.isf = isf_big;
     ab1.max_tiles = L.max_tiles_big;
-    KMOE_CK(launch_moe_gemm(true, kBigTileRows, kpsb1, mb1, ab1, grid, stream));
+    KMOE_CK(launch_moe_gemm(true, kBigTileRows, kpsb1, mb1, ab1, grid, stream, pdl));
   }
-  KMOE_CK(launch_moe_gemm(true, L.BN, kps1, m1, a1, grid, stream));
+  KMOE_CK(launch_moe_gemm(true, L.BN, kps1, m1, a1, grid, stream, pdl));
   KMOE_CK(mark(ev ? ev->fc1 : nullptr));
   GemmArgs a2{counts, seg_start, tile_start, w2_k, w2_k + weight_blocks(p, 1) * 8192, isf, E, H / 128, I / 128,
               L.max_tiles, H, I, nullptr, nullptr, 0.f, 0.f, 0.f, y, slot_of_row, err, kWaitBudgetNs,
@@ -410,11 +414,11 @@ static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* l
     ab2.tile_start = tile_start_big;
     ab2.bsf = isf_big;
     ab2.max_tiles = L.max_tiles_big;
-    KMOE_CK(launch_moe_gemm(false, kBigTileRows, kpsb2, mb2, ab2, grid, stream));
+    KMOE_CK(launch_moe_gemm(false, kBigTileRows, kpsb2, mb2, ab2, grid, stream, pdl));
   }
-  KMOE_CK(launch_moe_gemm(false, L.BN, kps2, m2, a2, grid, stream));
+  KMOE_CK(launch_moe_gemm(false, L.BN, kps2, m2, a2, grid, stream, pdl));
   KMOE_CK(mark(ev ? ev->fc2 : nullptr));
-  KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream));
+  KMOE_CK(launch_combine(y, ids, wts, T, H, k, E, p->routed_scaling_factor, out_bf16, stream, pdl));
   KMOE_CK(mark(ev ? ev->combined : nullptr));
   return KMOE_OK;
 }

@@ -13,6 +13,7 @@ namespace kmoe {
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ ids,
                                                       const float* __restrict__ w, int H, int k, int E, float rsf,
                                                       __nv_bfloat16* __restrict__ out) {
+  chain_wait();
   __shared__ float s_w[kMaxK];
   const int t = blockIdx.x;
   const int H4 = H / 4;
@@ -44,12 +45,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 cudaError_t launch_combine(const float* y, const int32_t* ids, const float* w, int T, int H, int k, int E, float rsf,
-                           void* out, cudaStream_t st) {
+                           void* out, cudaStream_t st, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int slices = (H / 4 + 255) / 256;
   const int split = T >= 1024 ? 1 : slices;  // few tokens: one block per (token, H slice)
-  combine_kernel<<<dim3(T, split), 256, 0, st>>>(y, ids, w, H, k, E, rsf, static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  return launch_chained(combine_kernel, dim3(T, split), dim3(256), 0, st, pdl, y, ids, w, H, k, E, rsf,
+                        static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace kmoe

@@ -24,6 +24,37 @@ __host__ inline int current_device() {
   return d;
 }
 
+// ---------------------------------------------------------------- launch chaining
+// The forward's kernels run back to back on one stream.  Each is launched
+// with programmatic stream serialization (pdl): it may start launching while
+// its predecessor still runs, so its CTAs are resident when the predecessor
+// ends.  Every kernel of the chain first waits until its predecessor grid has
+// completed and its memory is visible (griddepcontrol.wait returns at once
+// for a launch without that dependency), and only then lets its own
+// successor begin launching.  Nothing a kernel does precedes the wait, so the
+// stream order of every memory access is unchanged, and each grid completes
+// only after its predecessor: the order is transitive through the chain.
+__device__ __forceinline__ void chain_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+__host__ inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                           cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---------------------------------------------------------------- tile layout
 // Scales of the B operand (token rows) are stored per token tile so that a
 // tile's scales for one 128-wide K block form whole 512-byte blocks that

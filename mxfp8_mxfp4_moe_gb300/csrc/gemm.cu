@@ -97,6 +97,7 @@ struct GemmCfg {
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::CTAS_PER_SM) moe_gemm_kernel(const __grid_constant__ GemmMaps maps,
                                                                  const GemmArgs a) {
+  chain_wait();
   if (__ldg(a.tile_start + a.E) == 0) return;  // no tiles of this launch's class: leave before any set-up
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -392,7 +393,7 @@ cudaError_t launch_prep_weights(const uint8_t* codes, const uint8_t* sf, uint8_t
 
 // ---------------------------------------------------------------- launch
 template <class C>
-static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st) {
+static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& a, int grid, cudaStream_t st, bool pdl) {
   static bool attr_set[kMaxDevices] = {};  // per instantiation and device; benign race (idempotent)
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
@@ -401,28 +402,27 @@ static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& a, int grid,
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  moe_gemm_kernel<C><<<grid * C::CTAS_PER_SM, C::THREADS, C::SMEM, st>>>(maps, a);
-  return cudaGetLastError();
+  return launch_chained(moe_gemm_kernel<C>, dim3(grid * C::CTAS_PER_SM), dim3(C::THREADS), C::SMEM, st, pdl, maps, a);
 }
 
 cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, const GemmArgs& a, int grid,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool pdl) {
   if (a.KB % kps != 0) return cudaErrorInvalidValue;
   constexpr int PF = KMOE_DECODE_PF_STAGES;
   if (fc1) {
-    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, true, 4, 2, 1, PF>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<32, 1, 8, true, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
-    if (BN == 64 && kps == 1) return launch_one<GemmCfg<64, 1, 3, true, 4, 2, 1, 2 * PF>>(maps, a, grid, st);
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, true, 4, 2, 1, PF>>(maps, a, grid, st, pdl)
+                                  : launch_one<GemmCfg<32, 1, 8, true, 8, 1, 1, 2 * PF>>(maps, a, grid, st, pdl);
+    if (BN == 64 && kps == 1) return launch_one<GemmCfg<64, 1, 3, true, 4, 2, 1, 2 * PF>>(maps, a, grid, st, pdl);
     if (BN == 224 && kps == 1)
-      return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(true, maps, a, grid, st)
-                           : launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st);
+      return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(true, maps, a, grid, st, pdl)
+                           : launch_one<GemmCfg<224, 1, 4, true>>(maps, a, grid, st, pdl);
   } else {
-    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2, 1, PF>>(maps, a, grid, st)
-                                  : launch_one<GemmCfg<32, 1, 8, false, 8, 1, 1, 2 * PF>>(maps, a, grid, st);
-    if (BN == 64 && kps == 1) return launch_one<GemmCfg<64, 1, 4, false, 4, 2, 1, 2 * PF>>(maps, a, grid, st);
+    if (BN == 32) return kps == 2 ? launch_one<GemmCfg<32, 2, 2, false, 4, 2, 1, PF>>(maps, a, grid, st, pdl)
+                                  : launch_one<GemmCfg<32, 1, 8, false, 8, 1, 1, 2 * PF>>(maps, a, grid, st, pdl);
+    if (BN == 64 && kps == 1) return launch_one<GemmCfg<64, 1, 4, false, 4, 2, 1, 2 * PF>>(maps, a, grid, st, pdl);
     if (BN == 224 && kps == 1)
-      return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(false, maps, a, grid, st)
-                           : launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st);
+      return pair_gemm_supported(a.MT, a.KB) ? launch_moe_gemm_pair(false, maps, a, grid, st, pdl)
+                           : launch_one<GemmCfg<224, 1, 4, false>>(maps, a, grid, st, pdl);
   }
   return cudaErrorInvalidValue;
 }

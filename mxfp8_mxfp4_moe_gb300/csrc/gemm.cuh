@@ -54,13 +54,16 @@ cudaError_t launch_prep_weights(const uint8_t* codes, const uint8_t* sf, uint8_t
 // fc1: FC1 with the SiTU + MXFP8 requantisation epilogue; otherwise FC2 with
 // fp32 per-slot stores.  BN is the token-tile size of the layer (32, 64, 224).
 // kps must equal gemm_kblocks_per_stage(BN, a.KB) (the depth of maps.a's box).
+// pdl: launched with programmatic stream serialization (its predecessor on
+// the stream is a kernel of the same forward chain).
 cudaError_t launch_moe_gemm(bool fc1, int BN, int kps, const GemmMaps& maps, const GemmArgs& a, int grid,
-                            cudaStream_t st);
+                            cudaStream_t st, bool pdl);
 
 // The CTA-pair kernel for BN = 224 (gemm_pair.cu): weight tiles per expert
 // (MT) and K blocks (KB) must both be even.  `sms` is the SM count; the grid
 // is the number of co-resident pairs.
 bool pair_gemm_supported(int MT, int KB);
-cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st);
+cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st,
+                                 bool pdl);
 
 }  // namespace kmoe

@@ -88,6 +88,7 @@ constexpr int kShortKBlocks = 32;
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __grid_constant__ GemmMaps maps,
                                                                      const GemmArgs a) {
+  chain_wait();
   // no tiles of this launch's class: leave before any set-up (every CTA of
   // the cluster reads the same count)
   if (__ldg(a.tile_start + a.E) == 0) return;
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_pair_kernel(const __gr
 }
 
 template <class C>
-static cudaError_t launch_pair(const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
+static cudaError_t launch_pair(const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st, bool pdl) {
   static int pairs_of[kMaxDevices] = {};  // co-resident clusters of two (per instantiation and device)
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
@@ -427,30 +428,33 @@ static cudaError_t launch_pair(const GemmMaps& maps, const GemmArgs& a, int sms,
     pairs = n < sms / 2 ? n : sms / 2;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see chain_wait
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<C>, maps, a);
 }
 
 bool pair_gemm_supported(int MT, int KB) { return MT % 2 == 0 && KB % 2 == 0; }
 
-cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st) {
+cudaError_t launch_moe_gemm_pair(bool fc1, const GemmMaps& maps, const GemmArgs& a, int sms, cudaStream_t st,
+                                 bool pdl) {
   if (!pair_gemm_supported(a.MT, a.KB)) return cudaErrorInvalidValue;
   // FC1 claims items dynamically (in the fixed order its pairs finished up to
   // 4 % apart at H = 7168, and it is ahead at H = 3584 too); FC2's items do
   // better in the fixed order.
-  if (!fc1) return launch_pair<PairCfg<false, 3, false>>(maps, a, sms, st);
-  return a.KB <= kShortKBlocks ? launch_pair<PairCfg<true, 3, true, 8>>(maps, a, sms, st)
-                               : launch_pair<PairCfg<true, 3, true, 16>>(maps, a, sms, st);
+  if (!fc1) return launch_pair<PairCfg<false, 3, false>>(maps, a, sms, st, pdl);
+  return a.KB <= kShortKBlocks ? launch_pair<PairCfg<true, 3, true, 8>>(maps, a, sms, st, pdl)
+                               : launch_pair<PairCfg<true, 3, true, 16>>(maps, a, sms, st, pdl);
 }
 
 }  // namespace kmoe

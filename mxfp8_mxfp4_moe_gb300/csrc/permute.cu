@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(kRankChunk) rank_kernel(const int32_t* __restr
                                                           int32_t* __restrict__ rank,
                                                           int32_t* __restrict__ chunk_counts,
                                                           uint32_t* __restrict__ err) {
+  chain_wait();
   extern __shared__ int cnt[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ chunk_
                                                     int thr, int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ seg_start, int32_t* __restrict__ tile_start,
                                                     int32_t* __restrict__ tile_start_big) {
+  chain_wait();
   __shared__ int s_rows[1024];
   __shared__ int s_tiles[1024];
   __shared__ int s_big[1024];
@@ -137,6 +139,7 @@ __global__ void __launch_bounds__(kRankChunk) permute_small_kernel(const int32_t
                                                                    int32_t* __restrict__ tile_start_big,
                                                                    uint32_t* __restrict__ err) {
   static_assert(kRankChunk == 1024 && kMaxE <= kRankChunk, "one slot and one expert per thread, 32 warps");
+  chain_wait();
   __shared__ int cnt[kMaxE];
   __shared__ int w_rows[32], w_tiles[32], w_big[32];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
@@ -225,18 +228,16 @@ __global__ void __launch_bounds__(kRankChunk) permute_small_kernel(const int32_t
 
 cudaError_t launch_permute(const int32_t* ids, int R, int E, int BN, int thr, int32_t* rank, int32_t* chunk_prefix,
                            int32_t* counts, int32_t* seg_start, int32_t* tile_start, int32_t* tile_start_big,
-                           uint32_t* err, cudaStream_t st) {
+                           uint32_t* err, cudaStream_t st, bool pdl) {
   const int nchunk = (R + kRankChunk - 1) / kRankChunk;
-  if (nchunk <= 1) {
-    permute_small_kernel<<<1, kRankChunk, 0, st>>>(ids, R, E, BN, thr, rank, chunk_prefix, counts, seg_start,
-                                                   tile_start, tile_start_big, err);
-    return cudaGetLastError();
-  }
-  rank_kernel<<<nchunk, kRankChunk, E * sizeof(int), st>>>(ids, R, E, rank, chunk_prefix, err);
-  const cudaError_t e = cudaGetLastError();
+  if (nchunk <= 1)
+    return launch_chained(permute_small_kernel, dim3(1), dim3(kRankChunk), 0, st, pdl, ids, R, E, BN, thr, rank,
+                          chunk_prefix, counts, seg_start, tile_start, tile_start_big, err);
+  const cudaError_t e = launch_chained(rank_kernel, dim3(nchunk), dim3(kRankChunk), E * sizeof(int), st, pdl, ids, R,
+                                       E, rank, chunk_prefix, err);
   if (e != cudaSuccess) return e;
-  scan_kernel<<<1, 1024, 0, st>>>(chunk_prefix, nchunk, E, BN, thr, counts, seg_start, tile_start, tile_start_big);
-  return cudaGetLastError();
+  return launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, pdl, chunk_prefix, nchunk, E, BN, thr, counts,
+                        seg_start, tile_start, tile_start_big);
 }
 
 }  // namespace kmoe

@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(
     const int32_t* __restrict__ seg_start, const int32_t* __restrict__ tile_start,
     const int32_t* __restrict__ tile_start_big, int32_t* __restrict__ row_of_slot, int32_t* __restrict__ slot_of_row,
     uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf, uint8_t* __restrict__ xsf_big) {
+  chain_wait();
   __shared__ int s_row[kMaxK], s_tile[kMaxK], s_local[kMaxK], s_big[kMaxK];
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
@@ -199,12 +200,11 @@ cudaError_t launch_quant_scatter(const void* x, int T, int H, int k, int E, int 
                                  const int32_t* rank, const int32_t* chunk_prefix, const int32_t* counts,
                                  const int32_t* seg_start, const int32_t* tile_start, const int32_t* tile_start_big,
                                  int32_t* row_of_slot, int32_t* slot_of_row, uint8_t* xq, uint8_t* xsf,
-                                 uint8_t* xsf_big, cudaStream_t st) {
+                                 uint8_t* xsf_big, cudaStream_t st, bool pdl) {
   if (T == 0) return cudaSuccess;
-  quant_scatter_kernel<<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), H, k, E, BN, thr, ids, rank,
-                                          chunk_prefix, counts, seg_start, tile_start, tile_start_big, row_of_slot,
-                                          slot_of_row, xq, xsf, xsf_big);
-  return cudaGetLastError();
+  return launch_chained(quant_scatter_kernel, dim3(T), dim3(256), 0, st, pdl, static_cast<const __nv_bfloat16*>(x),
+                        H, k, E, BN, thr, ids, rank, chunk_prefix, counts, seg_start, tile_start, tile_start_big,
+                        row_of_slot, slot_of_row, xq, xsf, xsf_big);
 }
 
 }  // namespace kmoe

@@ -11,6 +11,7 @@ template <int KPL>
 __global__ void __launch_bounds__(32) route_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                                     int T, int E, int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ wts) {
+  chain_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
