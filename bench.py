@@ -393,10 +393,11 @@ def time_interleaved(layers, steps, dist, clocks, flush):
     return out, counts
 
 
-def time_graph(layer, steps):
+def time_graph(layer, steps, blocks=3):
     """The layer's forward captured once into a CUDA graph and replayed
-    `steps` times back to back (no host launch work between kernels);
-    microseconds per forward."""
+    `steps` times back to back (no host launch work between kernels), after
+    ten untimed replays; microseconds per forward, the median of `blocks`
+    such runs."""
     import torch
     st = torch.cuda.Stream()
     st.wait_stream(torch.cuda.current_stream())
@@ -406,17 +407,20 @@ def time_graph(layer, steps):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=st):
         layer.forward()
-    for _ in range(3):
+    for _ in range(10):
         g.replay()
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        g.replay()
-    e.record()
-    torch.cuda.synchronize()
-    return 1000.0 * s.elapsed_time(e) / steps
+    runs = []
+    for _ in range(blocks):
+        s.record()
+        for _ in range(steps):
+            g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        runs.append(1000.0 * s.elapsed_time(e) / steps)
+    return float(np.median(runs))
 
 
 def time_stages(layer, steps):
