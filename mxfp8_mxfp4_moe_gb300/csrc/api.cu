@@ -377,14 +377,11 @@ static int forward_impl(const kmoe_params* p, const void* x_bf16, const float* l
   }
   KMOE_CK(mark(ev ? ev->routed : nullptr));
   // Kernels after the first are chained (launch_chained): each may begin
-  // launching while its predecessor runs.  Not across stage events (their
-  // records sit between the kernels), nor after the copy of given ids, nor
-  // while the stream is captured into a graph (replays of the captured
-  // T=16 layer took 921 us with the chained launches, 884-891 without,
-  // against 862 us eager with them).
-  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
-  KMOE_CK(cudaStreamIsCapturing(stream, &capture));
-  const bool pdl = ev == nullptr && capture == cudaStreamCaptureStatusNone;
+  // launching while its predecessor runs (also inside a captured graph,
+  // where the T=16 layer replays in 857 us chained, 860 us not).  Not across
+  // stage events (their records sit between the kernels), nor after the copy
+  // of given ids.
+  const bool pdl = ev == nullptr;
   KMOE_CK(launch_permute(ids, R, E, L.BN, thr, rank, chunk_prefix, counts, seg_start, tile_start, tile_start_big, err,
                          stream, pdl && !given));
   KMOE_CK(mark(ev ? ev->permuted : nullptr));
