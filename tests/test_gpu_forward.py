@@ -209,10 +209,11 @@ def test_forward_expert_parallel_local_slice(K):
 
 @pytest.mark.parametrize("name", ["tiny", "reduced", "pair_tiles", "prefill"])
 def test_determinism_and_graph_replay(K, name):
-    """Three eager runs bitwise equal; a CUDA graph captured once and replayed
-    twice bitwise equal to them.  pair_tiles and prefill run the CTA-pair
-    GEMMs, whose FC1 work items are claimed dynamically (the order differs
-    from run to run, the result may not)."""
+    """Three eager runs bitwise equal; a run with stage events (its kernels
+    launched unchained) and a CUDA graph captured once and replayed twice
+    bitwise equal to them.  pair_tiles and prefill run the CTA-pair GEMMs,
+    whose FC1 work items are claimed dynamically (the order differs from run
+    to run, the result may not)."""
     for w in [{"pair_tiles": PAIR_EVEN}.get(name) or W.WORKLOADS[name]]:
         wt = device_weights(w)
         inp, s = device_inputs(w)
@@ -228,6 +229,15 @@ def test_determinism_and_graph_replay(K, name):
         torch.cuda.synchronize()
         for o in outs[1:]:
             assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+        # stage events between the kernels: the forward launches them unchained
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        for e in ev:
+            e.record()  # creates the event
+        o_ev = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+        K.kmoe_forward(p, inp["x"], inp["logits"], inp["bias"], wt["w13_k"], wt["w2_k"], out=o_ev, workspace=ws,
+                       stage_events=ev)
+        torch.cuda.synchronize()
+        assert torch.equal(o_ev.view(torch.int16), outs[0].view(torch.int16))
         # CUDA graph: capture once, replay twice, bitwise equal to eager
         g_out = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
         stream = torch.cuda.Stream()
