@@ -140,11 +140,15 @@ __device__ __forceinline__ float swiglu_f32(float g, float u, float alpha, float
 }
 
 // Epilogue staging tile: 128 rows x 32 floats, unpadded.  The 16-byte unit u
-// of row r is stored at unit u ^ (r & 7) ^ ((r >> 4) & 3), which keeps both
-// the row-wise float4 writes and the column reads of the SiTU step at most
-// two-way bank-conflicted.
+// of row r is stored at unit u ^ (r & 7) ^ ((r >> 3) & 7).  Row-wise float4
+// writes: any 8 consecutive lanes (rows) hit 8 distinct units.  Column reads
+// of the activation step: a warp reads, for one value index i, rows
+// UV*uu + i (and 64 + that) of 8 or 4 columns; the lane bits that select uu
+// (rows bits 3-5) and the column's unit reach the three unit bits through
+// the (r >> 3) term, and the column within the unit picks the bank inside
+// it, so the 32 lanes hit 32 distinct banks for both 8- and 16-value units.
 constexpr int kStgFloats = 128 * 32;
-__device__ __forceinline__ int stg_unit(int r, int u) { return r * 32 + ((u ^ (r & 7) ^ ((r >> 4) & 3)) << 2); }
+__device__ __forceinline__ int stg_unit(int r, int u) { return r * 32 + ((u ^ (r & 7) ^ ((r >> 3) & 7)) << 2); }
 __device__ __forceinline__ int stg_at(int r, int c) { return stg_unit(r, c >> 2) + (c & 3); }
 
 // One 32-column chunk (token columns c0..c0+31) of the 128 x BN accumulator
