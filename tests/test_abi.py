@@ -160,3 +160,52 @@ def test_binding_rejects_mis_sized_tensors_before_the_library(K):
     rejects(lambda: K.kmoe_router(x, wg, b, 2, workspace=torch.zeros(1, dtype=u8)), "workspace holds")
     rejects(lambda: K.kmoe_forward_router(p, x, torch.zeros(9, 128, dtype=bf), b, w13, w2), "w_gate")
     rejects(lambda: K.kmoe_device_error(torch.zeros(3, dtype=u8)), "workspace holds")
+
+
+def _worst_tiles(T, E, k, BN, big_rows, big_tile_rows):
+    """Adversarial per-expert row counts (each expert at most T rows, the sum
+    R = T*k, at most E experts) that maximise the tile count of each class:
+    small tiles favour many experts of 1, BN+1, 2BN+1, ... rows up to big_rows;
+    big tiles favour experts of big_rows+1 rows.  Returns (small, big)."""
+    R = T * k
+    small_cap = min(T, big_rows) if big_rows else T
+    # small class: one row per expert first, then BN more rows per extra tile
+    counts = [0] * E
+    left = R
+    for e in range(min(E, left)):
+        counts[e] = 1
+    left -= min(E, R)
+    grew = True
+    while left >= BN and grew:
+        grew = False
+        for e in range(E):
+            if left >= BN and counts[e] and counts[e] + BN <= small_cap:
+                counts[e] += BN
+                left -= BN
+                grew = True
+    small = sum(-(-c // BN) for c in counts if 0 < c <= (big_rows or T))
+    # big class: as many experts of big_rows + 1 rows as the rows and the experts allow
+    big = 0
+    if big_rows and T > big_rows:
+        n = min(E, R // (big_rows + 1))
+        big = n
+        extra = R - n * (big_rows + 1)
+        # more tiles on those experts: the next boundary (big_tile_rows + 1
+        # rows) first, then one tile per big_tile_rows, each expert at most T rows
+        step1 = big_tile_rows + 1 - (big_rows + 1)
+        if T >= big_tile_rows + 1 and step1 > 0:
+            first = min(n, extra // step1)
+            big += first
+            extra -= first * step1
+            per_expert = (T - (big_tile_rows + 1)) // big_tile_rows
+            big += min(extra // big_tile_rows, first * per_expert)
+    return small, big
+
+
+@pytest.mark.parametrize("T,E,k", [(8192, 896, 16), (2048, 896, 16), (128, 64, 16), (16, 896, 16), (16, 8, 2),
+                                   (65, 1024, 32), (300, 200, 8), (1, 1, 1), (64, 64, 16), (1000, 37, 5)])
+def test_workspace_tile_capacity_covers_adversarial_routing(K, T, E, k):
+    L = K.kmoe_workspace_layout(K.make_params(T, 128, 128, E, k))
+    small, big = _worst_tiles(T, E, k, L.tile_rows, L.big_rows if L.tile_rows_big else 0, 224)
+    assert small <= L.max_tiles, (small, L.max_tiles)
+    assert big <= (L.max_tiles_big if L.tile_rows_big else 0), (big, L.max_tiles_big)
